@@ -1,0 +1,529 @@
+"""Benchmark of the same-device collectives on one GB300 (or N replicas).
+
+The timed step is the DTensor redistribution Partial -> Shard(0) ->
+Replicate that the DTorch collective-communication page drives through
+ConvertKernel::ConvertPlacements (§2.5): a barrier, then ReduceScatter with
+kAvg, a barrier, then AllGatherIntoTensor, for P = 4 logical ranks that each
+hold a bf16 [8192, 4096] tensor on the same GPU.  The metric is collective
+HBM bandwidth: algorithmic bytes (every byte each kernel must read plus every
+byte it must write) over device time.
+
+One JSON line on rank 0.  Extra keys: roofline (dominant kernel, measured
+here with CUDA events on the launching stream, against the measured HBM copy
+peak), cpu_baseline (the CPU oracle on a bounded sample), e2e (the same step
+through the public API with pinned host buffers and the copies inside the
+timed region), clocks (nvidia-smi during the timed region), gpu_launches, and
+rows: one measurement per collective at its own workload (AllReduce P=2 fp32
+2^20; bucket all-reduce P=8 of 200 bf16 gradients; AllToAll and uneven
+AllGather P=8; barrier latency P=16).
+
+--impl reference times the CPU oracle on a bounded sample of the same workload
+instead (the reference arm; there is no other implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "collective HBM GB/s (and % of 8 TB/s) per op and size; barrier latency µs"
+UNIT = "GB/s"
+P_RANKS, ROWS, COLS = 4, 8192, 4096
+WORKLOAD = f"rs_avg_then_ag_bf16_P{P_RANKS}_{ROWS}x{COLS}"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu", "dt_math.cuh",
+                  "dt_internal.h"]
+
+
+# ----------------------------------------------------------------- helpers
+def step_bytes(P=P_RANKS, rows=ROWS, cols=COLS, es=2):
+    n = rows * cols                       # elements per rank
+    rs = P * n * es + n * es              # read P full inputs, write P shards (n total)
+    ag = n * es + P * n * es              # read P shards, write P full outputs
+    return rs, ag
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "same_device_collective_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, only while the
+    kernel sources are the ones the counters were taken on."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("src_sha") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        import datetime
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        mhz = sorted(r[1] for r in use)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside),
+                "window": "timed region" if inside else "whole run"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (identity at world size 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(local_ms: float, local_bytes: float, world: int, device=None):
+    """Whole-job throughput: bytes of all ranks over the slowest rank's time."""
+    ms = reduce_max(local_ms, world, device)
+    total = local_bytes * world
+    return ms, total / (ms * 1e-3) / 1e9
+
+
+# ----------------------------------------------------------- CPU oracle leg
+def oracle_sample_step(rows_per_rank: int, seed: int = 1):
+    """Build a bounded sample of the workload: P ranks of bf16
+    [rows_per_rank, COLS], same recipe as the full inputs."""
+    from same_device_collective_gb300 import workloads
+    import numpy as np
+    w = workloads.rs_ag(seed=seed, P=P_RANKS, rows=rows_per_rank, cols=COLS)
+    return [x.view(__import__("torch").int16).numpy().view(np.uint16).reshape(-1) for x in w.inputs]
+
+
+def time_oracle(rows_per_rank: int, min_seconds: float, max_reps: int):
+    import oracle
+    xs = oracle_sample_step(rows_per_rank)
+    rs_b, ag_b = step_bytes(rows=rows_per_rank)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        rs = oracle.reduce_scatter("bf16", "avg", xs)
+        oracle.all_gather(rs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return (rs_b + ag_b) * reps / el / 1e9, el, reps
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    rows = 32                                  # [32, 4096] bf16 per rank: 256 KiB
+    xs = oracle_sample_step(rows)
+    rs_b, ag_b = step_bytes(rows=rows)
+    for _ in range(args.warmup):
+        oracle.all_gather(oracle.reduce_scatter("bf16", "avg", xs))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.all_gather(oracle.reduce_scatter("bf16", "avg", xs))
+    el = time.perf_counter() - t0
+    value = (rs_b + ag_b) * args.steps / el / 1e9
+    sample = (f"{P_RANKS} ranks x bf16 [{rows}, {COLS}] per step, drawn with the workload's "
+              f"recipe (N(0,1), seed 1), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows_per_rank": rows, "P": P_RANKS},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def time_events(fn, iters, warmup=3):
+    """Median ms of fn over iters, CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for i in range(iters):
+        st[i].record()
+        fn()
+        en[i].record()
+    torch.cuda.synchronize()
+    ts = sorted(s.elapsed_time(e) for s, e in zip(st, en))
+    return ts[len(ts) // 2]
+
+
+def measure_rows(dt, dev, peak):
+    """One measurement per collective at its own workload (device-resident)."""
+    import torch
+    from same_device_collective_gb300 import workloads
+    rows = {}
+    ALL = dt.DT_ALL_RANKS
+
+    def rec(name, nbytes, ms, **extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2), "bytes": nbytes,
+                      "frac_of_measured_hbm": round(gbs / peak, 4),
+                      "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4), **extra}
+
+    # A1: AllReduce kSum, P=2, fp32 2^20 per rank (16 MiB moved: L2-resident, launch-bound)
+    w = workloads.allreduce_small()
+    xs = [x.to(dev) for x in w.inputs]
+    outs = [torch.empty_like(x) for x in xs]
+    g = dt.dt_group_create(2, dev.index)
+    n = xs[0].numel()
+    ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 200)
+    rec("allreduce_sum_f32_P2_n2^20", 2 * 2 * n * 4, ms, l2_resident=True)
+    dt.dt_group_destroy(g)
+    del xs, outs
+
+    # A1 at bandwidth scale: AllReduce kSum P=8 fp32, 64 MiB per rank
+    n = 16 << 20
+    gen = torch.Generator(device=dev).manual_seed(4)
+    xs = [torch.rand(n, generator=gen, device=dev) for _ in range(8)]
+    outs = [torch.empty_like(x) for x in xs]
+    g = dt.dt_group_create(8, dev.index)
+    ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 20)
+    rec("allreduce_sum_f32_P8_64MiB", 2 * 8 * n * 4, ms)
+    dt.dt_group_destroy(g)
+    del xs, outs
+
+    # A5: fused bucket all-reduce kAvg, P=8, 200 bf16 gradients, 25 MiB buckets
+    w = workloads.bucket_grads(device=str(dev))
+    counts = w.meta["counts"]
+    g = dt.dt_group_create(8, dev.index)
+    _, nb = dt.dt_bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
+    ms = time_events(lambda: dt.dt_bucket_allreduce(g, w.inputs, counts, "bf16", "avg",
+                                                    workloads.BUCKET_CAP_BYTES), 20)
+    rec("bucket_allreduce_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
+        barriers=nb - 1)
+    dt.dt_group_destroy(g)
+    del w
+
+    # A4: AllToAll P=8, bf16 [65536, 4096] per rank
+    w = workloads.all_to_all_tokens(device=str(dev))
+    outs = [torch.empty_like(x) for x in w.inputs]
+    g = dt.dt_group_create(8, dev.index)
+    nbytes_rank = w.inputs[0].numel() * 2
+    ms = time_events(lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes_rank // 8), 10)
+    rec("all_to_all_bf16_P8_65536x4096", 2 * 8 * nbytes_rank, ms)
+    dt.dt_group_destroy(g)
+    del w, outs
+
+    # A3b: uneven AllGather P=8, int32 rows U[1,16384] x 4096 (per-rank outputs)
+    w = workloads.uneven_gather(device=str(dev))
+    rws = w.meta["rows"]
+    total = sum(rws)
+    outs = [torch.empty(total, 4096, dtype=torch.int32, device=dev) for _ in range(8)]
+    g = dt.dt_group_create(8, dev.index)
+    ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4), 10)
+    rec("uneven_all_gather_i32_P8", total * 16384 * (1 + 8), ms, rows=rws)
+    dt.dt_group_destroy(g)
+    del outs
+    shared = torch.empty(total, 4096, dtype=torch.int32, device=dev)
+    g = dt.dt_group_create(8, dev.index)
+    ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, [shared] * 8, rws, 0, 4096 * 4,
+                                              flags=dt.DT_SHARED_OUTPUT), 10)
+    rec("uneven_all_gather_i32_P8_shared_output", total * 16384 * 2, ms)
+    dt.dt_group_destroy(g)
+    del w, shared
+
+    # A6: barrier latency, P=16, 10^5 back-to-back calls (and as a replayed CUDA graph)
+    g = dt.dt_group_create(16, dev.index)
+    calls = 100_000
+    for _ in range(100):
+        dt.dt_barrier(g)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(calls):
+        dt.dt_barrier(g)
+    e.record()
+    torch.cuda.synchronize()
+    us_direct = s.elapsed_time(e) * 1e3 / calls
+    us_graph = None
+    try:
+        stream = torch.cuda.Stream(dev)
+        per_graph = 1000
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(per_graph):
+                    dt.dt_barrier(g, stream=stream)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(calls // per_graph):
+            graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        us_graph = s.elapsed_time(e) * 1e3 / calls
+    except Exception as ex:   # capture support is reported, not required
+        us_graph = f"capture failed: {type(ex).__name__}"
+    win_ok = dt.dt_group_check(g) == dt.DT_OK
+    dt.dt_group_destroy(g)
+    rows["barrier_P16"] = {"us_per_call_stream": round(us_direct, 3),
+                           "us_per_call_graph": us_graph if isinstance(us_graph, str)
+                           else round(us_graph, 3), "calls": calls, "status_ok": win_ok}
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from same_device_collective_gb300 import dt, workloads
+
+    peak, peak_kind = measured_peak()
+    P, rows_, cols = P_RANKS, ROWS, COLS
+    w = workloads.rs_ag(seed=1, P=P, rows=rows_, cols=cols, device=str(dev))
+    xs = w.inputs
+    m = rows_ // P * cols
+    rs = [torch.empty(rows_ // P, cols, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    ag = [torch.empty(rows_, cols, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    g = dt.dt_group_create(P, local)
+    ALL = dt.DT_ALL_RANKS
+    rs_b, ag_b = step_bytes()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        dt.dt_barrier(g)
+        if ev is not None:
+            ev[0].record()
+        dt.dt_reduce_scatter(g, ALL, xs, rs, m, "bf16", "avg")
+        if ev is not None:
+            ev[1].record()
+        dt.dt_barrier(g)
+        if ev is not None:
+            ev[2].record()
+        dt.dt_all_gather(g, ALL, rs, ag, None, rows_ // P, cols * 2)
+        if ev is not None:
+            ev[3].record()
+
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = dt.dt_launch_count()
+    wall0 = time.time()
+    t_start.record()
+    for i in range(K):
+        step(evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    launches = dt.dt_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    local_ms = t_start.elapsed_time(t_end)
+    ms, value = aggregate(local_ms, (rs_b + ag_b) * K, world, dev)
+    rs_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    ag_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    assert dt.dt_group_check(g) == dt.DT_OK
+
+    if rs_ms >= ag_ms:
+        dom, dom_bytes, dom_ms, key = "reduce_scatter (reduce_vec_kernel<bf16,avg,P<=4>)", rs_b, rs_ms, "reduce_scatter"
+    else:
+        dom, dom_bytes, dom_ms, key = "all_gather (copy_vec_kernel)", ag_b, ag_ms, "all_gather"
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(key),
+                "kernel": dom, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": round(dom_ms * 1e3, 2),
+                "per_kernel": {
+                    "reduce_scatter": {"bytes": rs_b, "avg_us": round(rs_ms * 1e3, 2),
+                                       "GB/s": round(rs_b / (rs_ms * 1e-3) / 1e9, 1)},
+                    "all_gather": {"bytes": ag_b, "avg_us": round(ag_ms * 1e3, 2),
+                                   "GB/s": round(ag_b / (ag_ms * 1e-3) / 1e9, 1)}}}
+
+    # e2e: same step through the public API, inputs from pinned host memory and
+    # the gathered result read back, copies inside the timed region
+    h_in = [x.cpu().pin_memory() for x in xs]
+    h_out = [torch.empty(rows_, cols, dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    e2e_steps = max(3, min(K, 50))
+
+    def e2e_step():
+        for d, h in zip(xs, h_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(h_out, ag):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record()
+    torch.cuda.synchronize()
+    e2e_ms, e2e_value = aggregate(s0.elapsed_time(s1), (rs_b + ag_b) * e2e_steps, world, dev)
+    h2d = sum(x.numel() * 2 for x in xs)
+    d2h = sum(x.numel() * 2 for x in ag)
+
+    rows_out = None
+    if args.rows and world == 1:
+        dt.dt_group_destroy(g)
+        g = None
+        del h_in, h_out
+        rows_out = measure_rows(dt, dev, peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, el, reps = time_oracle(1024, min_seconds=10.0, max_reps=50)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"RS(avg)+AG on {P} ranks x bf16 [1024, {COLS}] (1/8 of the workload's "
+                         f"rows, drawn with the same recipe), {reps} reps in {el:.1f} s, "
+                         f"single-threaded C"}
+
+    if g is not None:
+        dt.dt_group_destroy(g)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms / K, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "P": P, "rows": rows_, "cols": cols,
+                       "op": "avg", "accumulate": "fp32",
+                       "step": "barrier, reduce_scatter(avg), barrier, all_gather",
+                       "bytes_per_step": rs_b + ag_b, "outputs": "per-rank",
+                       "l2": "inputs larger than L2 (256 MiB of inputs per step vs 126.5 MB L2)",
+                       "parallelism": f"replicas x{world}, P={P} logical ranks per GPU"},
+            "frac_of_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": round(e2e_ms / e2e_steps, 4)},
+            "gpu_launches": launches,
+            "clocks": clocks.summary(wall0, wall1),
+        }
+        if rows_out is not None:
+            line["rows"] = rows_out
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", dest="rows", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,215 @@
+/*
+ * dt.h -- collectives among P logical ranks that share one GPU.
+ *
+ * The operation set is the ThreadGroup collective set of the DTorch developer
+ * guide page "集合通信组件" (collective communication component): §2.1 lists
+ * the ThreadGroup methods (AllReduce, AllGatherIntoTensor, AllGather with
+ * uneven shards, ReduceScatterTensor, AllToAll, Barrier) and §2.3 describes
+ * ThreadGroupSameDeviceBackend, the backend used when every rank of the group
+ * lives on the same GPU.  On top of that set come the fused gradient-bucket
+ * all-reduce with 1/P scaling of "异步融合 AllReduce 流水线优化" (MindSpore
+ * hyper-parallel issue #120, AllReduceParamGroup) and the notify/wait barrier
+ * of "Barrier：仅信号（Signals Only）" (PyPTO distributed tutorial).
+ *
+ * Group-wide calls.  One call carries every rank's buffer (rank ==
+ * DT_ALL_RANKS, pointer arrays with P entries) and runs as one kernel that
+ * reads all P rank buffers directly from HBM.  Per-rank calls (rank >= 0, one
+ * host thread per rank) are reserved and return DT_ERR_UNSUPPORTED.
+ *
+ * Conventions shared by every entry point:
+ *   Streams   `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *             default stream).  A call enqueues its work on `stream` and
+ *             returns without waiting for the GPU, like a collective in
+ *             synchronous mode on the PyTorch page "通信与互联（05）" §四.2:
+ *             results are valid in stream order.  Inputs must be produced in
+ *             stream order, or the caller makes `stream` wait on an event.
+ *   Buffers   Device pointers.  The caller owns them and keeps them alive
+ *             until `stream` has passed the call (§五.5 of the same page).
+ *             The group owns only its signal window, error word and plan
+ *             scratch, allocated once by dt_group_create.
+ *   Alignment Any alignment is accepted.  When every pointer and size is a
+ *             multiple of 16 bytes the kernels move 16-byte vectors; otherwise
+ *             they fall back to element-wise access with identical results.
+ *   Errors    Argument errors are reported before anything is enqueued.  A
+ *             device-side wait that runs out of time records DT_ERR_TIMEOUT
+ *             in the group's error word; that code is returned by the next
+ *             call on the group (and by dt_group_check), and the group then
+ *             refuses work until dt_group_reset.  No call throws.
+ *   Numerics  fp32 and bf16 reduce in fp32 registers, combining ranks in
+ *             ascending rank order (rank 0 first, as the same-device
+ *             AllReduce adds ranks 1..P-1 onto rank 0's tensor in order); bf16
+ *             is rounded once, to nearest even, at the store; AVG divides the
+ *             fp32 sum by P with IEEE division; int32 sums wrap modulo 2^32;
+ *             MAX/MIN select an input element (a NaN wins; on equal values
+ *             the lower rank's element is kept).
+ */
+#ifndef DT_H
+#define DT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dt_group *dt_group_t;
+
+typedef enum {
+    DT_OK = 0,
+    DT_ERR_INVALID = 1,      /* bad argument; nothing was enqueued */
+    DT_ERR_UNSUPPORTED = 2,  /* legal request this build does not do (AVG on int32, ...) */
+    DT_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+    DT_ERR_TIMEOUT = 4,      /* a device-side wait ran out of time (see dt_group_check) */
+    DT_ERR_OOM = 5,          /* the group could not allocate its own state */
+    DT_ERR_POISONED = 6      /* an earlier timeout left the group unusable until reset */
+} dt_status;
+
+typedef enum { DT_F32 = 0, DT_BF16 = 1, DT_I32 = 2 } dt_dtype;
+
+/* ReduceOpType of the ThreadGroup interface: kSum, kAvg, kMax, kMin. */
+typedef enum { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2, DT_MIN = 3 } dt_redop;
+
+#define DT_MAX_RANKS 16
+#define DT_ALL_RANKS (-1)
+/* Flag: every out[] entry names the same buffer; the result is written once.
+ * The same-device AllReduce hands all ranks one shared result tensor. */
+#define DT_SHARED_OUTPUT 0x1u
+/* Default bucket cap: DDP's bucket_cap_mb = 25, read as 25 MiB. */
+#define DT_DEFAULT_BUCKET_CAP_BYTES ((size_t)25 << 20)
+
+/* ------------------------------------------------------------------ groups */
+
+/* Create a group of world_size (1..DT_MAX_RANKS) logical ranks on CUDA device
+ * cuda_device.  Allocates the P x P int32 signal window, the error word and
+ * the plan scratch on that device, so every later call is allocation-free.
+ * The device-side wait limit is read from the environment variable
+ * DT_TIMEOUT_MS (default 2000).  Like the TensorStore constructor, which
+ * starts all participants from one state, the window starts at zero.
+ * Returns DT_ERR_INVALID for a bad size or NULL out, DT_ERR_CUDA / DT_ERR_OOM
+ * on a failed CUDA call (nothing is leaked). */
+dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out);
+
+/* Wait for the group's outstanding work, then free everything it owns. */
+dt_status dt_group_destroy(dt_group_t g);
+
+/* TensorStore::Reset analogue: zero the signal window and the error word on
+ * `stream`, wait for that stream, clear the poisoned state and restart the
+ * barrier generation at 0.  Blocks the calling thread. */
+dt_status dt_group_reset(dt_group_t g, void *stream);
+
+/* Report the first device-side error recorded so far without synchronising:
+ * DT_OK, or the recorded code (the group is poisoned from then on).
+ * rank/peer/generation of the failed wait are returned when the pointers are
+ * not NULL. */
+dt_status dt_group_check(dt_group_t g);
+dt_status dt_group_error_detail(dt_group_t g, int *rank, int *peer, int *generation);
+
+/* Number of ranks; number of barriers issued since create/reset. */
+int dt_group_size(dt_group_t g);
+int64_t dt_group_generation(dt_group_t g);
+
+/* Change the device-side wait limit of later calls (milliseconds, >= 1). */
+dt_status dt_group_set_timeout_ms(dt_group_t g, uint32_t timeout_ms);
+
+const char *dt_status_string(dt_status st);
+
+/* Kernels this library has launched in this process (all groups). */
+uint64_t dt_launch_count(void);
+
+/* ------------------------------------------------------------- collectives */
+
+/* AllReduce (P -> R): "集合通信组件" §2.1 AllReduce(input, reduceOpType) and
+ * the three-phase same-device AllReduce of §2.3.
+ *   in[r]   rank r's `count` elements of `dtype` (P entries)
+ *   out[q]  rank q's result, `count` elements (P entries); out[q] may equal
+ *           in[q] (in place).  With DT_SHARED_OUTPUT all out[] are one buffer
+ *           written once; it may not overlap any input.
+ * out[q][i] = scale( in[0][i] op in[1][i] op ... op in[P-1][i] ), scale = 1/P
+ * for DT_AVG.  DT_AVG on DT_I32 -> DT_ERR_UNSUPPORTED. */
+dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *const *out,
+                       size_t count, int dtype, int op, unsigned flags, void *stream);
+
+/* ReduceScatter (P -> S(0)): "集合通信组件" §2.1 ReduceScatterTensor.
+ *   in[r]   rank r's P * recv_count elements: shard s is elements
+ *           [s * recv_count, (s + 1) * recv_count) (dim 0 split evenly)
+ *   out[r]  recv_count elements: the reduction over all ranks of shard r.
+ * Outputs may not overlap inputs. */
+dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void *const *out,
+                            size_t recv_count, int dtype, int op, void *stream);
+
+/* AllGather (S(0) -> R): "集合通信组件" §2.1 AllGatherIntoTensor (equal
+ * shards, rows == NULL: every rank has rows_equal rows) and AllGather with
+ * uneven shards (rows[r] rows on rank r).  Rows are row_bytes bytes; rank r's
+ * rows land at row offset rows[0] + ... + rows[r-1] of every out[q], which
+ * holds the sum of all rows.  With DT_SHARED_OUTPUT every out[] is one buffer
+ * written once.  Byte copies: any element type. */
+dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *const *out,
+                        const size_t *rows, size_t rows_equal, size_t row_bytes,
+                        unsigned flags, void *stream);
+
+/* AllToAll (S -> S, split and concatenated along dim 0): "集合通信组件"
+ * §2.1 AllToAll.  in[i] is P chunks of chunk_bytes; chunk j of rank i goes
+ * to rank j, which stacks what it receives in ascending source rank:
+ *   out[j][i * chunk_bytes + k] = in[i][j * chunk_bytes + k]. */
+dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *const *out,
+                        size_t chunk_bytes, void *stream);
+
+/* Fused gradient-bucket all-reduce: "异步融合 AllReduce 流水线优化"
+ * (AllReduceParamGroup.issue_async_allreduce / wait_and_apply_grads: SUM
+ * all-reduce of the fused gradient buffer, each gradient view then divided by
+ * the replicate world size for AVG) with the bucketing of "通信与互联（05）"
+ * §六.5 (DDP gathers gradients into bucket_cap_mb = 25 MB buckets).
+ *   grads[t * P + p]  rank p's gradient t, counts[t] elements, updated in place
+ *   dtype             DT_BF16 or DT_F32;  op  DT_SUM or DT_AVG
+ *   bucket_cap_bytes  0 -> DT_DEFAULT_BUCKET_CAP_BYTES
+ * Tensors are grouped in order into buckets (dt_bucket_plan); each bucket is
+ * one kernel that reads and writes the gradients in place through a chunk
+ * table (no flatten copy), and one signal-window barrier (dt_barrier) runs
+ * between consecutive buckets.  The plan table is staged through the group's
+ * scratch; at most one bucket call per group may be in flight. */
+dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *counts,
+                              size_t n_tensors, int dtype, int op, size_t bucket_cap_bytes,
+                              void *stream);
+
+/* The bucket plan used above, on the host only (no GPU needed): greedy in the
+ * given order, a bucket closes when the next tensor would take it past
+ * cap_bytes, a tensor larger than the cap gets a bucket of its own.
+ * bucket_of[t] receives tensor t's bucket; *n_buckets the bucket count. */
+dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_bytes,
+                         size_t cap_bytes, size_t *bucket_of, size_t *n_buckets);
+
+/* Signal-window barrier: "Barrier：仅信号（Signals Only）".  The group keeps
+ * an int32 window win[P][P] in HBM (row r of rank q's window is win[q][r]).
+ * The g-th barrier (1-based generation, bumped by every call) is one kernel
+ * with one thread block per rank: rank r adds 1 (AtomicAdd, release) to
+ * win[q][r] of every peer q != r, then waits until win[r][s] >= g (Ge,
+ * acquire) for every s != r.  Afterwards win[r][s] == g for s != r and
+ * win[r][r] == 0.  Each wait gives up after the group's time limit and
+ * records DT_ERR_TIMEOUT. */
+dt_status dt_barrier(dt_group_t g, int rank, void *stream);
+
+/* ------------------------------------------------------------- test hooks */
+
+/* Copy the P x P window to host_out (row-major, win[q][r] at q * P + r) after
+ * the work already on `stream`; blocks the calling thread. */
+dt_status dt_debug_read_window(dt_group_t g, int32_t *host_out, void *stream);
+
+/* The ordering example of the barrier page (built-in reveal): one kernel,
+ * one block per rank; rank r copies in[r] to stage[r], passes the barrier,
+ * then copies stage[(r + 1) % P] to out[r].  Each buffer holds `bytes`. */
+dt_status dt_debug_ring_after_barrier(dt_group_t g, const void *const *in,
+                                      void *const *stage, void *const *out, size_t bytes,
+                                      void *stream);
+
+/* Failure injection for tests: run one barrier kernel whose waits expect the
+ * generation current + extra (extra >= 1), which no rank will reach, with a
+ * wait limit of timeout_ms.  The waits give up, DT_ERR_TIMEOUT is recorded
+ * in the error word and the kernel returns; the GPU stays usable. */
+dt_status dt_debug_barrier_expect(dt_group_t g, int extra, uint32_t timeout_ms, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DT_H */

@@ -1,0 +1,148 @@
+// Signal-window barrier among the P ranks of a group, and the ordering test
+// kernel built on it.
+//
+// The PyPTO page "Barrier：仅信号（Signals Only）" builds an N-rank barrier from
+// two primitives: notify adds 1 (AtomicAdd) to a cell of a peer's signal
+// window, wait blocks until a cell of one's own window reaches a threshold
+// (Ge).  Rank r notifies every peer q != r at row r of q's window and then
+// waits on every row s != r of its own window; a rank never notifies itself,
+// so its own row stays 0.  Because the counters only grow, every reuse of the
+// window raises the threshold: the g-th barrier waits for g.
+//
+// Here the window is int32 win[P][P] in HBM (win[q][r] is row r of rank q's
+// window) and the ranks are the P blocks of one cooperative launch, so all of
+// them are resident together.  Lane q of block r's first warp notifies peer
+// q with a release reduction and then polls row q of rank r's window with
+// acquire loads.  The generation is kept per rank on the device (rank_gen),
+// so a captured and replayed launch still raises the threshold each time.
+// Every poll loop ends after the group's time limit (or an iteration bound);
+// a rank that gives up records DT_ERR_TIMEOUT once in the error word and its
+// host-mapped mirror and returns, so the GPU is never held.
+#include "dt_internal.h"
+
+namespace dt {
+namespace {
+
+__device__ __forceinline__ void notify_add(int32_t *cell)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(cell), "r"(1) : "memory");
+}
+
+__device__ __forceinline__ int32_t load_acquire(const int32_t *cell)
+{
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cell) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ void record_error(const BarrierParams &p, int code, int rank, int peer, int gen)
+{
+    if (atomicCAS(&p.err->code, 0, code) == 0) {
+        p.err->rank = rank;
+        p.err->peer = peer;
+        p.err->gen = gen;
+        volatile DevError *h = p.err_host;
+        h->rank = rank;
+        h->peer = peer;
+        h->gen = gen;
+        __threadfence_system();
+        h->code = code;
+        __threadfence_system();
+    }
+}
+
+// Run by the 32 lanes of one warp for rank r; true when every wait ended in time.
+__device__ bool rank_barrier(const BarrierParams &p, int r)
+{
+    const int lane = threadIdx.x & 31;
+    const int P = p.P;
+    const int32_t g = p.rank_gen[r] + 1;
+    const bool peer = lane < P && lane != r;
+
+    __threadfence();                     // this rank's earlier writes before its notifies
+    if (peer) notify_add(&p.win[lane * P + r]);
+
+    bool ok = true;
+    if (peer) {
+        const int32_t want = g + p.extra;
+        const uint64_t t0 = global_ns();
+        const uint64_t max_polls = p.timeout_ns / 256 + 4096;
+        uint32_t sleep_ns = 0;
+        for (uint64_t it = 0;; ++it) {
+            const int32_t v = load_acquire(&p.win[r * P + lane]);
+            if ((int32_t)(v - want) >= 0) break;          // Ge, safe across wrap-around
+            if (it >= max_polls || global_ns() - t0 > p.timeout_ns) { ok = false; break; }
+            if (it >= 64) {
+                sleep_ns = sleep_ns ? (sleep_ns < 256 ? sleep_ns * 2 : 256) : 32;
+                __nanosleep(sleep_ns);
+            }
+        }
+    }
+    __threadfence();                     // peers' writes before this rank's later reads
+    const unsigned bad = __ballot_sync(0xFFFFFFFFu, !ok);
+    if (lane == 0) {
+        if (bad) record_error(p, DT_ERR_TIMEOUT, r, __ffs(bad) - 1, g);
+        p.rank_gen[r] = g;
+    }
+    __syncwarp();
+    return bad == 0;
+}
+
+__global__ void __launch_bounds__(32) barrier_kernel(const __grid_constant__ BarrierParams p)
+{
+    rank_barrier(p, blockIdx.x);
+}
+
+__device__ void copy_bytes(unsigned char *dst, const unsigned char *src, uint64_t n)
+{
+    const bool vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | n) & 15) == 0;
+    if (vec) {
+        const uint4 *s = reinterpret_cast<const uint4 *>(src);
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        for (uint64_t i = threadIdx.x; i < n / 16; i += blockDim.x) d[i] = s[i];
+    } else {
+        for (uint64_t i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+    }
+}
+
+// The barrier page's ordering example: stage, barrier, read the next rank.
+__global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ RingParams p)
+{
+    __shared__ int ok;
+    const int r = blockIdx.x;
+    copy_bytes(p.stage[r], p.in[r], p.bytes);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const bool passed = rank_barrier(p.bar, r);
+        if (threadIdx.x == 0) ok = passed;
+    }
+    __syncthreads();
+    if (ok) copy_bytes(p.out[r], p.stage[(r + 1) % p.bar.P], p.bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s)
+{
+    void *args[] = {const_cast<BarrierParams *>(&p)};
+    count_launch();
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(barrier_kernel),
+                                       dim3(p.P), dim3(32), args, 0, s);
+}
+
+cudaError_t launch_ring(const RingParams &p, cudaStream_t s)
+{
+    void *args[] = {const_cast<RingParams *>(&p)};
+    count_launch();
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel),
+                                       dim3(p.bar.P), dim3(kThreads), args, 0, s);
+}
+
+}  // namespace dt

@@ -1,0 +1,730 @@
+// Host side of the same-device collective library: the group object,
+// argument validation, launch planning and the C ABI entry points.
+//
+// DTorch's same-device backend ("集合通信组件" §2.3, §3.4) moves every
+// collective through a TensorStore: each rank thread publishes its tensor
+// under a key (SrcSet, which records a CUDA event), consumers wait on that
+// event (DestGet), and two host barriers (Reset) close every operation.  A
+// group-wide call here plays all of those roles at once: the P rank pointers
+// the caller passes are the store's slots, they travel to the device as the
+// kernel's parameter block (or, for buckets, as a table staged in HBM), and
+// ordering is the order of the caller's stream.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include "dt_internal.h"
+
+namespace dt {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count(int device)
+{
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(device);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+        n = 1;
+    cache[device] = n;
+    return n;
+}
+
+cudaError_t resident_blocks(const void *fn, int threads, int device, int *out)
+{
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    const uint64_t key = reinterpret_cast<uintptr_t>(fn) * 131u + (uint64_t)device * 7u + threads;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) { *out = it->second; return cudaSuccess; }
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0);
+    if (e != cudaSuccess) return e;
+    const int n = sm_count(device) * (per_sm > 0 ? per_sm : 1);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+}  // namespace dt
+
+namespace {
+
+using dt::DevError;
+
+size_t elem_bytes(int dtype) { return dtype == DT_BF16 ? 2 : 4; }
+bool valid_dtype(int dtype) { return dtype == DT_F32 || dtype == DT_BF16 || dtype == DT_I32; }
+bool valid_op(int op) { return op >= DT_SUM && op <= DT_MIN; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Switch to the group's device for the duration of a call.
+struct DeviceScope {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceScope(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceScope()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+struct Range {
+    uintptr_t lo, hi;   // [lo, hi)
+    int rank;
+    int kind;           // 0 input, 1 output
+};
+
+bool overlaps(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Status of a call that finds an error recorded by the device.
+dt_status take_device_error(dt_group *g)
+{
+    if (g->poisoned) return DT_ERR_POISONED;
+    const int code = static_cast<volatile DevError *>(g->h_err)->code;
+    if (code != 0) {
+        g->poisoned = true;
+        g->poison_code = static_cast<dt_status>(code);
+        return static_cast<dt_status>(code);
+    }
+    return DT_OK;
+}
+
+dt_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return DT_OK;
+    if (e == cudaErrorMemoryAllocation) return DT_ERR_OOM;
+    return DT_ERR_CUDA;
+}
+
+dt_status check_rank(dt_group *g, int rank)
+{
+    if (rank == DT_ALL_RANKS) return DT_OK;
+    if (rank >= 0 && rank < g->P) return DT_ERR_UNSUPPORTED;   // per-rank calls: reserved
+    return DT_ERR_INVALID;
+}
+
+bool is_pow2(int P) { return P > 0 && (P & (P - 1)) == 0; }
+
+void set_avg(int P, float *scale, int32_t *pow2)
+{
+    *pow2 = is_pow2(P);
+    *scale = *pow2 ? 1.0f / (float)P : 0.0f;   // exact for powers of two
+}
+
+dt::BarrierParams barrier_params(dt_group *g, int extra, uint64_t timeout_ns)
+{
+    dt::BarrierParams b;
+    b.win = g->d_win;
+    b.rank_gen = g->d_win + (size_t)g->P * g->P;
+    b.err = g->d_err;
+    b.err_host = g->h_err_dev;
+    b.timeout_ns = timeout_ns;
+    b.P = g->P;
+    b.extra = extra;
+    return b;
+}
+
+uint64_t timeout_ns(const dt_group *g) { return (uint64_t)g->timeout_ms * 1000000ull; }
+
+dt_status issue_barrier(dt_group *g, cudaStream_t s)
+{
+    const dt::BarrierParams b = barrier_params(g, 0, timeout_ns(g));
+    cudaError_t e = dt::launch_barrier(b, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    g->barriers_issued++;
+    return DT_OK;
+}
+
+void release_plan_slot(dt_group *g, int k)
+{
+    if (g->h_plan[k]) cudaFreeHost(g->h_plan[k]);
+    if (g->d_plan[k]) cudaFree(g->d_plan[k]);
+    g->h_plan[k] = nullptr;
+    g->d_plan[k] = nullptr;
+    g->plan_bytes[k] = 0;
+}
+
+void destroy_all(dt_group *g)
+{
+    for (int k = 0; k < dt_group::kPlanSlots; ++k) {
+        release_plan_slot(g, k);
+        if (g->plan_done[k]) cudaEventDestroy(g->plan_done[k]);
+    }
+    if (g->d_win) cudaFree(g->d_win);
+    if (g->d_err) cudaFree(g->d_err);
+    if (g->h_err) cudaFreeHost(g->h_err);
+    delete g;
+}
+
+cudaError_t grow_plan_slot(dt_group *g, int k, size_t bytes)
+{
+    if (bytes <= g->plan_bytes[k]) return cudaSuccess;
+    size_t cap = g->plan_bytes[k] ? g->plan_bytes[k] : ((size_t)1 << 20);
+    while (cap < bytes) cap *= 2;
+    release_plan_slot(g, k);
+    cudaError_t e = cudaHostAlloc(&g->h_plan[k], cap, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_plan[k], cap);
+    if (e != cudaSuccess) { release_plan_slot(g, k); return e; }
+    g->plan_bytes[k] = cap;
+    return cudaSuccess;
+}
+
+// Greedy bucket plan shared by dt_bucket_plan and dt_bucket_allreduce.
+size_t plan_buckets(const size_t *counts, size_t T, size_t es, size_t cap, size_t *bucket_of)
+{
+    size_t b = 0, filled = 0;
+    for (size_t t = 0; t < T; ++t) {
+        const size_t bytes = counts[t] * es;
+        if (filled > 0 && filled + bytes > cap) { ++b; filled = 0; }
+        bucket_of[t] = b;
+        filled += bytes;
+    }
+    return T ? b + 1 : 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dt_status_string(dt_status st)
+{
+    switch (st) {
+    case DT_OK: return "ok";
+    case DT_ERR_INVALID: return "invalid argument";
+    case DT_ERR_UNSUPPORTED: return "unsupported";
+    case DT_ERR_CUDA: return "CUDA error";
+    case DT_ERR_TIMEOUT: return "device wait timed out";
+    case DT_ERR_OOM: return "out of memory";
+    case DT_ERR_POISONED: return "group poisoned by an earlier device error; reset it";
+    }
+    return "unknown status";
+}
+
+uint64_t dt_launch_count(void) { return dt::g_launches.load(std::memory_order_relaxed); }
+
+dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
+{
+    if (!out) return DT_ERR_INVALID;
+    *out = nullptr;
+    if (world_size < 1 || world_size > DT_MAX_RANKS || cuda_device < 0) return DT_ERR_INVALID;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return DT_ERR_CUDA;
+    if (cuda_device >= ndev) return DT_ERR_INVALID;
+    DeviceScope scope(cuda_device);
+    if (!scope.ok) return DT_ERR_CUDA;
+
+    dt_group *g = new (std::nothrow) dt_group;
+    if (!g) return DT_ERR_OOM;
+    g->P = world_size;
+    g->device = cuda_device;
+    if (const char *env = std::getenv("DT_TIMEOUT_MS")) {
+        const long v = std::strtol(env, nullptr, 10);
+        if (v >= 1 && v <= 3600000) g->timeout_ms = (uint32_t)v;
+    }
+    const size_t win_bytes = ((size_t)world_size * world_size + world_size) * sizeof(int32_t);
+    cudaError_t e = cudaMalloc(&g->d_win, win_bytes);
+    if (e == cudaSuccess) e = cudaMemset(g->d_win, 0, win_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_err, sizeof(DevError));
+    if (e == cudaSuccess) e = cudaMemset(g->d_err, 0, sizeof(DevError));
+    if (e == cudaSuccess) e = cudaHostAlloc(&g->h_err, sizeof(DevError), cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+        memset(g->h_err, 0, sizeof(DevError));
+        e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&g->h_err_dev), g->h_err, 0);
+    }
+    for (int k = 0; k < dt_group::kPlanSlots && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&g->plan_done[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = grow_plan_slot(g, k, (size_t)1 << 20);
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        destroy_all(g);
+        return cuda_status(e);
+    }
+    *out = g;
+    return DT_OK;
+}
+
+dt_status dt_group_destroy(dt_group_t g)
+{
+    if (!g) return DT_ERR_INVALID;
+    DeviceScope scope(g->device);
+    for (int k = 0; k < dt_group::kPlanSlots; ++k)
+        if (g->plan_used[k]) cudaEventSynchronize(g->plan_done[k]);
+    cudaDeviceSynchronize();
+    destroy_all(g);
+    return DT_OK;
+}
+
+dt_status dt_group_reset(dt_group_t g, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t win_bytes = ((size_t)g->P * g->P + g->P) * sizeof(int32_t);
+    cudaError_t e = cudaMemsetAsync(g->d_win, 0, win_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(g->d_err, 0, sizeof(DevError), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    memset(g->h_err, 0, sizeof(DevError));
+    g->poisoned = false;
+    g->poison_code = DT_OK;
+    g->barriers_issued = 0;
+    return DT_OK;
+}
+
+dt_status dt_group_check(dt_group_t g)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const dt_status st = take_device_error(g);
+    return g->poisoned ? g->poison_code : st;
+}
+
+dt_status dt_group_error_detail(dt_group_t g, int *rank, int *peer, int *generation)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    volatile DevError *h = g->h_err;
+    if (rank) *rank = h->rank;
+    if (peer) *peer = h->peer;
+    if (generation) *generation = h->gen;
+    return static_cast<dt_status>(h->code);
+}
+
+int dt_group_size(dt_group_t g) { return g ? g->P : 0; }
+
+int64_t dt_group_generation(dt_group_t g) { return g ? g->barriers_issued : -1; }
+
+dt_status dt_group_set_timeout_ms(dt_group_t g, uint32_t timeout_ms)
+{
+    if (!g || timeout_ms < 1) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->timeout_ms = timeout_ms;
+    return DT_OK;
+}
+
+dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_bytes_,
+                         size_t cap_bytes, size_t *bucket_of, size_t *n_buckets)
+{
+    if (!n_buckets || (n_tensors && (!counts || !bucket_of)) || elem_bytes_ == 0 || cap_bytes == 0)
+        return DT_ERR_INVALID;
+    for (size_t t = 0; t < n_tensors; ++t)
+        if (counts[t] > SIZE_MAX / elem_bytes_) return DT_ERR_INVALID;
+    *n_buckets = plan_buckets(counts, n_tensors, elem_bytes_, cap_bytes, bucket_of);
+    return DT_OK;
+}
+
+dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *const *out,
+                       size_t count, int dtype, int op, unsigned flags, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if ((st = check_rank(g, rank)) != DT_OK) return st;
+    if (!in || !out || !valid_dtype(dtype) || !valid_op(op) || (flags & ~DT_SHARED_OUTPUT))
+        return DT_ERR_INVALID;
+    if (dtype == DT_I32 && op == DT_AVG) return DT_ERR_UNSUPPORTED;
+    if (count > SIZE_MAX / 16) return DT_ERR_INVALID;
+    const int P = g->P;
+    const bool shared = flags & DT_SHARED_OUTPUT;
+    const size_t bytes = count * elem_bytes(dtype);
+    for (int r = 0; r < P; ++r)
+        if (!in[r] || !out[r]) return DT_ERR_INVALID;
+    if (shared)
+        for (int r = 1; r < P; ++r)
+            if (out[r] != out[0]) return DT_ERR_INVALID;
+    if (count == 0) return DT_OK;
+
+    // Outputs may alias only their own rank's input exactly (in place), never
+    // another buffer; a shared output aliases nothing.
+    const int nout = shared ? 1 : P;
+    for (int q = 0; q < nout; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + bytes, q, 1};
+        for (int r = 0; r < P; ++r) {
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + bytes, r, 0};
+            if (overlaps(o, i) && (shared || r != q || in[r] != out[q])) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < nout; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + bytes, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+
+    dt::ReduceParams p;
+    memset(&p, 0, sizeof p);
+    bool vec = true;
+    for (int r = 0; r < P; ++r) {
+        p.in[r] = in[r];
+        vec = vec && aligned16(in[r]);
+    }
+    for (int q = 0; q < nout; ++q) {
+        p.out[q] = out[q];
+        vec = vec && aligned16(out[q]);
+    }
+    p.n = count;
+    p.job_stride = 0;
+    p.P = P;
+    p.out_per_job = nout;
+    set_avg(P, &p.avg_scale, &p.avg_pow2);
+
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_reduce(p, dtype, op, 1, vec, g->device,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void *const *out,
+                            size_t recv_count, int dtype, int op, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if ((st = check_rank(g, rank)) != DT_OK) return st;
+    if (!in || !out || !valid_dtype(dtype) || !valid_op(op)) return DT_ERR_INVALID;
+    if (dtype == DT_I32 && op == DT_AVG) return DT_ERR_UNSUPPORTED;
+    const int P = g->P;
+    if (recv_count > SIZE_MAX / 16 / (size_t)P) return DT_ERR_INVALID;
+    for (int r = 0; r < P; ++r)
+        if (!in[r] || !out[r]) return DT_ERR_INVALID;
+    if (recv_count == 0) return DT_OK;
+    const size_t es = elem_bytes(dtype);
+    const size_t in_bytes = recv_count * P * es, out_bytes = recv_count * es;
+    for (int q = 0; q < P; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + out_bytes, q, 1};
+        for (int r = 0; r < P; ++r) {
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + in_bytes, r, 0};
+            if (overlaps(o, i)) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < P; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + out_bytes, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+
+    dt::ReduceParams p;
+    memset(&p, 0, sizeof p);
+    const size_t epv = 16 / es;
+    bool vec = recv_count % epv == 0;
+    for (int r = 0; r < P; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = out[r];
+        vec = vec && aligned16(in[r]) && aligned16(out[r]);
+    }
+    p.n = recv_count;
+    p.job_stride = recv_count;
+    p.P = P;
+    p.out_per_job = 1;
+    set_avg(P, &p.avg_scale, &p.avg_pow2);
+
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_reduce(p, dtype, op, P, vec, g->device,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *const *out,
+                        const size_t *rows, size_t rows_equal, size_t row_bytes, unsigned flags,
+                        void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if ((st = check_rank(g, rank)) != DT_OK) return st;
+    if (!in || !out || (flags & ~DT_SHARED_OUTPUT)) return DT_ERR_INVALID;
+    const int P = g->P;
+    const bool shared = flags & DT_SHARED_OUTPUT;
+    size_t nrows[DT_MAX_RANKS], off[DT_MAX_RANKS], total = 0;
+    for (int r = 0; r < P; ++r) {
+        nrows[r] = rows ? rows[r] : rows_equal;
+        if (row_bytes && nrows[r] > SIZE_MAX / 4 / row_bytes) return DT_ERR_INVALID;
+        off[r] = total;
+        total += nrows[r];
+        if (total > SIZE_MAX / 4 / (row_bytes ? row_bytes : 1)) return DT_ERR_INVALID;
+    }
+    for (int r = 0; r < P; ++r)
+        if (!out[r] || (nrows[r] && !in[r])) return DT_ERR_INVALID;
+    if (shared)
+        for (int r = 1; r < P; ++r)
+            if (out[r] != out[0]) return DT_ERR_INVALID;
+    const size_t out_bytes = total * row_bytes;
+    if (out_bytes == 0) return DT_OK;
+    const int nout = shared ? 1 : P;
+    for (int q = 0; q < nout; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + out_bytes, q, 1};
+        for (int r = 0; r < P; ++r) {
+            if (!nrows[r]) continue;
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + nrows[r] * row_bytes, r, 0};
+            if (overlaps(o, i)) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < nout; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + out_bytes, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+
+    dt::CopySeg segs[DT_MAX_RANKS];
+    bool vec = true;
+    for (int r = 0; r < P; ++r) {
+        segs[r].src = static_cast<const unsigned char *>(in[r]);
+        segs[r].bytes = nrows[r] * row_bytes;
+        segs[r].dst_off = off[r] * row_bytes;
+        segs[r].tile_begin = 0;
+        segs[r].dst_first = 0;
+        segs[r].dst_count = nout;
+        if (segs[r].bytes)
+            vec = vec && aligned16(in[r]) && segs[r].bytes % 16 == 0 && segs[r].dst_off % 16 == 0;
+    }
+    void *outs[DT_MAX_RANKS] = {};
+    for (int q = 0; q < nout; ++q) {
+        outs[q] = out[q];
+        vec = vec && aligned16(out[q]);
+    }
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_copy(segs, P, outs, vec, g->device,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *const *out,
+                        size_t chunk_bytes, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if ((st = check_rank(g, rank)) != DT_OK) return st;
+    if (!in || !out) return DT_ERR_INVALID;
+    const int P = g->P;
+    if (chunk_bytes > SIZE_MAX / 4 / (size_t)P) return DT_ERR_INVALID;
+    for (int r = 0; r < P; ++r)
+        if (!in[r] || !out[r]) return DT_ERR_INVALID;
+    if (chunk_bytes == 0) return DT_OK;
+    const size_t bytes = chunk_bytes * P;
+    for (int q = 0; q < P; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + bytes, q, 1};
+        for (int r = 0; r < P; ++r) {
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + bytes, r, 0};
+            if (overlaps(o, i)) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < P; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + bytes, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+
+    // segment (i, j): chunk j of rank i -> rank j at offset i * chunk_bytes;
+    // ordered by source rank so that each block streams one input in order
+    std::vector<dt::CopySeg> segs((size_t)P * P);
+    bool vec = chunk_bytes % 16 == 0;
+    for (int i = 0; i < P; ++i) {
+        vec = vec && aligned16(in[i]) && aligned16(out[i]);
+        for (int j = 0; j < P; ++j) {
+            dt::CopySeg &sg = segs[(size_t)i * P + j];
+            sg.src = static_cast<const unsigned char *>(in[i]) + (size_t)j * chunk_bytes;
+            sg.bytes = chunk_bytes;
+            sg.dst_off = (size_t)i * chunk_bytes;
+            sg.tile_begin = 0;
+            sg.dst_first = j;
+            sg.dst_count = 1;
+        }
+    }
+    void *outs[DT_MAX_RANKS] = {};
+    for (int q = 0; q < P; ++q) outs[q] = out[q];
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, vec, g->device,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *counts,
+                              size_t n_tensors, int dtype, int op, size_t bucket_cap_bytes,
+                              void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (dtype != DT_BF16 && dtype != DT_F32) return valid_dtype(dtype) ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
+    if (op != DT_SUM && op != DT_AVG) return valid_op(op) ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
+    if (n_tensors && (!grads || !counts)) return DT_ERR_INVALID;
+    if (n_tensors > (1u << 30)) return DT_ERR_INVALID;
+    const int P = g->P;
+    const size_t es = elem_bytes(dtype);
+    const size_t cap = bucket_cap_bytes ? bucket_cap_bytes : DT_DEFAULT_BUCKET_CAP_BYTES;
+
+    // validate and find overlapping gradient buffers (sorted sweep)
+    std::vector<Range> ranges;
+    ranges.reserve(n_tensors * P);
+    size_t nchunks = 0;
+    for (size_t t = 0; t < n_tensors; ++t) {
+        if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
+        if (counts[t] == 0) continue;
+        for (int p = 0; p < P; ++p) {
+            const void *ptr = grads[t * P + p];
+            if (!ptr) return DT_ERR_INVALID;
+            ranges.push_back({(uintptr_t)ptr, (uintptr_t)ptr + counts[t] * es, p, 1});
+        }
+        nchunks += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
+    }
+    std::sort(ranges.begin(), ranges.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].lo < ranges[i - 1].hi) return DT_ERR_INVALID;
+    if (nchunks == 0) return DT_OK;
+    if (nchunks > 0x7FFFFFFFu) return DT_ERR_INVALID;
+
+    std::vector<size_t> bucket_of(n_tensors);
+    const size_t nb = plan_buckets(counts, n_tensors, es, cap, bucket_of.data());
+
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // plan layout: [T * P pointers][chunks]; buckets own consecutive chunk runs
+    const size_t ptr_bytes = n_tensors * P * sizeof(void *);
+    const size_t plan_bytes = ptr_bytes + nchunks * sizeof(dt::BucketChunk);
+    const int k = g->next_plan;
+    g->next_plan = (k + 1) % dt_group::kPlanSlots;
+    cudaError_t e = cudaSuccess;
+    if (g->plan_used[k]) e = cudaEventSynchronize(g->plan_done[k]);
+    if (e == cudaSuccess) e = grow_plan_slot(g, k, plan_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+
+    unsigned char *h = static_cast<unsigned char *>(g->h_plan[k]);
+    memcpy(h, grads, ptr_bytes);
+    dt::BucketChunk *chunks = reinterpret_cast<dt::BucketChunk *>(h + ptr_bytes);
+    // buckets hold consecutive tensors, so chunks in tensor order are grouped
+    // by bucket; bucket_begin[b] is the first chunk of bucket b
+    std::vector<uint32_t> bucket_begin(nb + 1, 0);
+    for (size_t t = 0; t < n_tensors; ++t)
+        bucket_begin[bucket_of[t] + 1] +=
+            (uint32_t)((counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems);
+    for (size_t b = 0; b < nb; ++b) bucket_begin[b + 1] += bucket_begin[b];
+    size_t c = 0;
+    for (size_t t = 0; t < n_tensors; ++t) {
+        bool al = true;
+        for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
+        for (size_t beg = 0; beg < counts[t]; beg += dt::kBucketChunkElems) {
+            const size_t n = std::min<size_t>(dt::kBucketChunkElems, counts[t] - beg);
+            chunks[c].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
+            chunks[c].nelem = (uint32_t)n;
+            chunks[c].begin = beg;
+            ++c;
+        }
+    }
+
+    e = cudaMemcpyAsync(g->d_plan[k], h, plan_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    const unsigned char *d = static_cast<const unsigned char *>(g->d_plan[k]);
+
+    dt::BucketParams bp;
+    bp.ptrs = reinterpret_cast<void *const *>(d);
+    bp.P = P;
+    set_avg(P, &bp.avg_scale, &bp.avg_pow2);
+    for (size_t b = 0; b < nb; ++b) {
+        bp.chunks = reinterpret_cast<const dt::BucketChunk *>(d + ptr_bytes) + bucket_begin[b];
+        bp.nchunks = bucket_begin[b + 1] - bucket_begin[b];
+        e = dt::launch_bucket(bp, dtype, op, g->device, s);
+        if (e != cudaSuccess) break;
+        if (b + 1 < nb) {
+            st = issue_barrier(g, s);
+            if (st != DT_OK) return st;
+        }
+    }
+    cudaError_t e2 = cudaEventRecord(g->plan_done[k], s);
+    g->plan_used[k] = true;
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(e2);
+}
+
+dt_status dt_barrier(dt_group_t g, int rank, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if ((st = check_rank(g, rank)) != DT_OK) return st;
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return issue_barrier(g, static_cast<cudaStream_t>(stream));
+}
+
+dt_status dt_debug_read_window(dt_group_t g, int32_t *host_out, void *stream)
+{
+    if (!g || !host_out) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_out, g->d_win, (size_t)g->P * g->P * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+dt_status dt_debug_ring_after_barrier(dt_group_t g, const void *const *in, void *const *stage,
+                                      void *const *out, size_t bytes, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (!in || !stage || !out) return DT_ERR_INVALID;
+    const int P = g->P;
+    dt::RingParams rp;
+    memset(&rp, 0, sizeof rp);
+    for (int r = 0; r < P; ++r) {
+        if (bytes && (!in[r] || !stage[r] || !out[r])) return DT_ERR_INVALID;
+        rp.in[r] = static_cast<const unsigned char *>(in[r]);
+        rp.stage[r] = static_cast<unsigned char *>(stage[r]);
+        rp.out[r] = static_cast<unsigned char *>(out[r]);
+    }
+    rp.bytes = bytes;
+    rp.bar = barrier_params(g, 0, timeout_ns(g));
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    cudaError_t e = dt::launch_ring(rp, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    g->barriers_issued++;
+    return DT_OK;
+}
+
+dt_status dt_debug_barrier_expect(dt_group_t g, int extra, uint32_t timeout_ms, void *stream)
+{
+    if (!g || extra < 1 || timeout_ms < 1 || timeout_ms > 10000) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    const dt::BarrierParams b = barrier_params(g, extra, (uint64_t)timeout_ms * 1000000ull);
+    cudaError_t e = dt::launch_barrier(b, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    g->barriers_issued++;
+    return DT_OK;
+}
+
+}  // extern "C"

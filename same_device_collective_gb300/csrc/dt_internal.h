@@ -1,0 +1,149 @@
+// Internal declarations of the same-device collective library: kernel
+// parameter blocks, launchers and the group object.  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "dt.h"
+
+namespace dt {
+
+constexpr int kThreads = 256;                          // threads per block, all data kernels
+constexpr int kMaxSeg = DT_MAX_RANKS * DT_MAX_RANKS;   // all-to-all: P^2 chunk copies
+constexpr int kCopyTileBytes = 16384;                  // one block moves 16 KiB per tile
+constexpr uint32_t kBucketChunkElems = 32768;          // bucket work unit, elements
+
+// First device-side failure, written once (atomicCAS on code) by the kernel
+// that hit it, mirrored into host-mapped memory so the host can read it
+// without synchronising.
+struct DevError {
+    int32_t code;
+    int32_t rank;
+    int32_t peer;
+    int32_t gen;
+};
+
+// ---- reduction (AllReduce, ReduceScatter) ---------------------------------
+// Job j (blockIdx.y) reduces elements [j * job_stride, j * job_stride + n)
+// of every input and writes them to out[j * out_per_job + k], k < out_per_job.
+// AllReduce: 1 job, out_per_job = P (or 1 shared).  ReduceScatter: P jobs,
+// out_per_job = 1, job_stride = n.
+struct ReduceParams {
+    const void *in[DT_MAX_RANKS];
+    void *out[DT_MAX_RANKS];
+    uint64_t n;
+    uint64_t job_stride;
+    float avg_scale;     // AVG with P a power of two: exact 1/P
+    int32_t avg_pow2;    // 1: multiply by avg_scale (same rounding as /P); 0: divide by P
+    int32_t P;
+    int32_t out_per_job;
+};
+
+// ---- byte copies (AllGather, AllToAll) ------------------------------------
+// Segment s copies `bytes` from src to out[dst_first + k] + dst_off for
+// k < dst_count; segments are cut into tiles of tile_bytes and tile t of the
+// launch belongs to the segment with tile_begin <= t < next tile_begin.
+struct CopySeg {
+    const unsigned char *src;
+    uint64_t bytes;
+    uint64_t dst_off;
+    uint64_t tile_begin;
+    int32_t dst_first;
+    int32_t dst_count;
+};
+
+template <int NSEG>
+struct CopyParams {
+    void *out[DT_MAX_RANKS];
+    uint64_t tile_bytes;
+    uint64_t total_tiles;
+    int32_t nseg;
+    int32_t pad;
+    CopySeg seg[NSEG];
+};
+
+// ---- fused bucket all-reduce ----------------------------------------------
+// One chunk = up to kBucketChunkElems elements of one tensor.  slot indexes
+// the tensor's row of P pointers in `ptrs`; bit 31 of slot marks a tensor
+// whose P pointers are all 16-byte aligned (vector path).
+struct BucketChunk {
+    uint32_t slot;
+    uint32_t nelem;
+    uint64_t begin;
+};
+
+struct BucketParams {
+    const BucketChunk *chunks;
+    void *const *ptrs;   // [n_slots][P]
+    uint32_t nchunks;
+    int32_t P;
+    float avg_scale;
+    int32_t avg_pow2;
+};
+
+// ---- barrier ----------------------------------------------------------------
+struct BarrierParams {
+    int32_t *win;        // [P][P]
+    int32_t *rank_gen;   // [P]: barriers rank r has passed
+    DevError *err;       // device error word
+    DevError *err_host;  // device view of the host-mapped mirror
+    uint64_t timeout_ns;
+    int32_t P;
+    int32_t extra;       // added to the threshold (failure injection); 0 normally
+};
+
+struct RingParams {
+    BarrierParams bar;
+    const unsigned char *in[DT_MAX_RANKS];
+    unsigned char *stage[DT_MAX_RANKS];
+    unsigned char *out[DT_MAX_RANKS];
+    uint64_t bytes;
+};
+
+// ---- launchers (one per kernel family; each counts its launches) ----------
+void count_launch();
+int sm_count(int device);
+// SMs x blocks of `fn` one SM holds at once (cached per kernel and device).
+cudaError_t resident_blocks(const void *fn, int threads, int device, int *out);
+
+cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bool vec,
+                          int device, cudaStream_t s);
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec,
+                        int device, cudaStream_t s);
+cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s);
+cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s);
+cudaError_t launch_ring(const RingParams &p, cudaStream_t s);
+
+}  // namespace dt
+
+// The group object behind dt_group_t.
+struct dt_group {
+    int P = 0;
+    int device = 0;
+    uint32_t timeout_ms = 2000;
+    int64_t barriers_issued = 0;
+    bool poisoned = false;
+    dt_status poison_code = DT_OK;
+
+    int32_t *d_win = nullptr;        // [P][P] window followed by rank_gen[P]
+    dt::DevError *d_err = nullptr;
+    dt::DevError *h_err = nullptr;   // host-mapped mirror (host view)
+    dt::DevError *h_err_dev = nullptr;
+
+    // bucket plan staging: kPlanSlots pinned host buffers and device buffers,
+    // each reused only after its event says the last kernel reading it ended
+    static constexpr int kPlanSlots = 2;
+    void *h_plan[kPlanSlots] = {nullptr, nullptr};
+    void *d_plan[kPlanSlots] = {nullptr, nullptr};
+    size_t plan_bytes[kPlanSlots] = {0, 0};
+    cudaEvent_t plan_done[kPlanSlots] = {nullptr, nullptr};
+    bool plan_used[kPlanSlots] = {false, false};
+    int next_plan = 0;
+
+    std::mutex mu;
+};

@@ -1,0 +1,170 @@
+// Element arithmetic of the reducing collectives, shared by the AllReduce /
+// ReduceScatter kernel and the fused bucket kernel.
+//
+// Ranks are combined in ascending order, rank 0 first: the same-device
+// AllReduce of the DTorch collective-communication page (§2.3) starts from
+// rank 0's tensor and adds ranks 1..P-1 onto it in turn.  fp32 and bf16
+// accumulate in fp32 (bf16 widens exactly), with one round-to-nearest-even
+// narrowing at the store; AVG divides the fp32 sum by P (the hyper-parallel
+// page divides each reduced gradient by the replicate world size); int32
+// sums wrap.  MAX / MIN select an input element: a NaN wins, equal values
+// keep the lower rank's element.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "dt.h"
+
+namespace dt {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x -> low half, .y -> high half
+    uint32_t w;
+    memcpy(&w, &h, sizeof w);
+    return w;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float f)
+{
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    uint16_t b;
+    memcpy(&b, &h, sizeof b);
+    return b;
+}
+
+__device__ __forceinline__ float avg_of(float sum, int P, float scale, int pow2)
+{
+    // For P = 2^k, sum * 2^-k and sum / P are the same real number and round
+    // identically; other P take the IEEE division.
+    return pow2 ? __fmul_rn(sum, scale) : __fdiv_rn(sum, (float)P);
+}
+
+template <int OP>
+__device__ __forceinline__ bool take_f(float x, float best)
+{
+    return (x != x) || (OP == DT_MAX ? x > best : x < best);
+}
+
+template <int OP>
+__device__ __forceinline__ int32_t pick_i(int32_t acc, int32_t x)
+{
+    if (OP == DT_SUM) return (int32_t)((uint32_t)acc + (uint32_t)x);
+    if (OP == DT_MAX) return x > acc ? x : acc;
+    return x < acc ? x : acc;
+}
+
+// Reduce one 16-byte vector position across the first P of PMAX rank vectors.
+template <int DT, int OP, int PMAX>
+__device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, float scale, int pow2)
+{
+    uint32_t w[PMAX][4];
+#pragma unroll
+    for (int r = 0; r < PMAX; ++r) {
+        w[r][0] = x[r].x; w[r][1] = x[r].y; w[r][2] = x[r].z; w[r][3] = x[r].w;
+    }
+    uint32_t o[4];
+    if constexpr (DT == DT_I32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            int32_t acc = (int32_t)w[0][k];
+#pragma unroll
+            for (int r = 1; r < PMAX; ++r)
+                if (r < P) acc = pick_i<OP>(acc, (int32_t)w[r][k]);
+            o[k] = (uint32_t)acc;
+        }
+    } else if constexpr (DT == DT_F32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float acc = __uint_as_float(w[0][k]);
+#pragma unroll
+            for (int r = 1; r < PMAX; ++r) {
+                if (r < P) {
+                    float x1 = __uint_as_float(w[r][k]);
+                    if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x1);
+                    else acc = take_f<OP>(x1, acc) ? x1 : acc;
+                }
+            }
+            if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
+            o[k] = __float_as_uint(acc);
+        }
+    } else {  // bf16: two elements per 32-bit word, low half first
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (OP == DT_SUM || OP == DT_AVG) {
+                float lo = bf16_lo(w[0][k]), hi = bf16_hi(w[0][k]);
+#pragma unroll
+                for (int r = 1; r < PMAX; ++r) {
+                    if (r < P) {
+                        lo = __fadd_rn(lo, bf16_lo(w[r][k]));
+                        hi = __fadd_rn(hi, bf16_hi(w[r][k]));
+                    }
+                }
+                if constexpr (OP == DT_AVG) {
+                    lo = avg_of(lo, P, scale, pow2);
+                    hi = avg_of(hi, P, scale, pow2);
+                }
+                o[k] = pack_bf16x2(lo, hi);
+            } else {
+                uint32_t blo = w[0][k] & 0xFFFFu, bhi = w[0][k] >> 16;
+                float flo = bf16_lo(w[0][k]), fhi = bf16_hi(w[0][k]);
+#pragma unroll
+                for (int r = 1; r < PMAX; ++r) {
+                    if (r < P) {
+                        const float xl = bf16_lo(w[r][k]), xh = bf16_hi(w[r][k]);
+                        if (take_f<OP>(xl, flo)) { flo = xl; blo = w[r][k] & 0xFFFFu; }
+                        if (take_f<OP>(xh, fhi)) { fhi = xh; bhi = w[r][k] >> 16; }
+                    }
+                }
+                o[k] = blo | (bhi << 16);
+            }
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Element-wise form: reduce element in_off + i of each rank buffer base[r]
+// and store it as element i of dst[k], k < ndst.  Used for ragged tails and
+// unaligned buffers.
+template <int DT, int OP>
+__device__ __forceinline__ void reduce_elem(const void *const *base, uint64_t in_off, uint64_t i,
+                                            int P, void *const *dst, int ndst, float scale,
+                                            int pow2)
+{
+    const uint64_t j = in_off + i;
+    if constexpr (DT == DT_I32) {
+        int32_t acc = static_cast<const int32_t *>(base[0])[j];
+        for (int r = 1; r < P; ++r) acc = pick_i<OP>(acc, static_cast<const int32_t *>(base[r])[j]);
+        for (int k = 0; k < ndst; ++k) static_cast<int32_t *>(dst[k])[i] = acc;
+    } else if constexpr (DT == DT_F32) {
+        float acc = static_cast<const float *>(base[0])[j];
+        for (int r = 1; r < P; ++r) {
+            const float x = static_cast<const float *>(base[r])[j];
+            if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x);
+            else acc = take_f<OP>(x, acc) ? x : acc;
+        }
+        if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
+        for (int k = 0; k < ndst; ++k) static_cast<float *>(dst[k])[i] = acc;
+    } else {
+        uint16_t b = static_cast<const uint16_t *>(base[0])[j];
+        float acc = bf16_to_f32(b);
+        for (int r = 1; r < P; ++r) {
+            const uint16_t xb = static_cast<const uint16_t *>(base[r])[j];
+            const float x = bf16_to_f32(xb);
+            if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x);
+            else if (take_f<OP>(x, acc)) { acc = x; b = xb; }
+        }
+        if constexpr (OP == DT_SUM || OP == DT_AVG) {
+            if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
+            b = f32_to_bf16(acc);
+        }
+        for (int k = 0; k < ndst; ++k) static_cast<uint16_t *>(dst[k])[i] = b;
+    }
+}
+
+}  // namespace dt

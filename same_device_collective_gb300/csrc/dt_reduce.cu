@@ -1,0 +1,148 @@
+// One-pass reduction kernel for AllReduce and ReduceScatter among P ranks on
+// one GPU.
+//
+// The same-device AllReduce of the DTorch collective-communication page
+// (§2.3) publishes every rank's tensor and lets rank 0 add ranks 1..P-1 onto
+// its own, one add kernel per rank, before handing the result back.  Here a
+// single launch reads all P rank buffers straight from HBM: each thread loads
+// its 16-byte vector from every rank before combining them (P x U loads in
+// flight per thread), reduces in registers in ascending rank order, and
+// stores the result to every destination.  HBM traffic is the algorithmic
+// minimum: P reads and (number of outputs) writes per vector position.
+//
+// Grid: blockIdx.y is the job (1 for AllReduce, P for ReduceScatter), and
+// blockIdx.x strides over the job's vectors; the launcher caps the grid at
+// the number of blocks the SMs hold at once, so every block is resident.
+#include "dt_internal.h"
+#include "dt_math.cuh"
+
+namespace dt {
+namespace {
+
+template <int PMAX>
+struct Unroll {   // 16 loads of 16 bytes in flight per thread
+    static constexpr int U = PMAX >= 16 ? 1 : 16 / PMAX;
+};
+
+template <int DT, int OP, int PMAX>
+__global__ void __launch_bounds__(kThreads)
+reduce_vec_kernel(const __grid_constant__ ReduceParams p)
+{
+    constexpr int U = Unroll<PMAX>::U;
+    constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
+    const int P = p.P;
+    const int j = blockIdx.y;
+    const uint64_t nvec = p.n / EPV;
+    const uint64_t in_off = (uint64_t)j * (p.job_stride / EPV);
+    const uint64_t step = (uint64_t)gridDim.x * kThreads * U;
+    void *const *dst = p.out + j * p.out_per_job;
+    const int ndst = p.out_per_job;
+
+    for (uint64_t base = (uint64_t)blockIdx.x * kThreads * U + threadIdx.x; base < nvec;
+         base += step) {
+        uint4 x[U][PMAX];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = base + (uint64_t)u * kThreads;
+            if (v < nvec) {
+#pragma unroll
+                for (int r = 0; r < PMAX; ++r)
+                    if (r < P) x[u][r] = __ldcg(static_cast<const uint4 *>(p.in[r]) + in_off + v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = base + (uint64_t)u * kThreads;
+            if (v < nvec) {
+                const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
+                for (int k = 0; k < ndst; ++k) __stcg(static_cast<uint4 *>(dst[k]) + v, y);
+            }
+        }
+    }
+
+    // ragged tail: the last n % EPV elements of the job, element by element
+    if (blockIdx.x == 0) {
+        const uint64_t in_elem_off = (uint64_t)j * p.job_stride;
+        for (uint64_t i = nvec * EPV + threadIdx.x; i < p.n; i += kThreads)
+            reduce_elem<DT, OP>(p.in, in_elem_off, i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+    }
+}
+
+// Any alignment: element by element, same arithmetic.
+template <int DT, int OP>
+__global__ void __launch_bounds__(kThreads)
+reduce_scalar_kernel(const __grid_constant__ ReduceParams p)
+{
+    const int j = blockIdx.y;
+    const uint64_t in_elem_off = (uint64_t)j * p.job_stride;
+    void *const *dst = p.out + j * p.out_per_job;
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n;
+         i += (uint64_t)gridDim.x * kThreads)
+        reduce_elem<DT, OP>(p.in, in_elem_off, i, p.P, dst, p.out_per_job, p.avg_scale, p.avg_pow2);
+}
+
+using ReduceFn = void (*)(ReduceParams);
+
+struct KernelInfo {
+    ReduceFn fn = nullptr;
+    int per_vec_iter = 1;   // vectors (or elements) per thread per iteration
+};
+
+template <int DT, int OP>
+KernelInfo pick_vec(int P)
+{
+    KernelInfo k;
+    if (P <= 2) { k.fn = reduce_vec_kernel<DT, OP, 2>; k.per_vec_iter = Unroll<2>::U; }
+    else if (P <= 4) { k.fn = reduce_vec_kernel<DT, OP, 4>; k.per_vec_iter = Unroll<4>::U; }
+    else if (P <= 8) { k.fn = reduce_vec_kernel<DT, OP, 8>; k.per_vec_iter = Unroll<8>::U; }
+    else { k.fn = reduce_vec_kernel<DT, OP, 16>; k.per_vec_iter = Unroll<16>::U; }
+    return k;
+}
+
+template <int DT>
+KernelInfo pick_op(int op, int P, bool vec)
+{
+    KernelInfo k;
+    switch (op) {
+    case DT_SUM: k = vec ? pick_vec<DT, DT_SUM>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_SUM>, 1}; break;
+    case DT_MAX: k = vec ? pick_vec<DT, DT_MAX>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_MAX>, 1}; break;
+    case DT_MIN: k = vec ? pick_vec<DT, DT_MIN>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_MIN>, 1}; break;
+    case DT_AVG:
+        if constexpr (DT != DT_I32)
+            k = vec ? pick_vec<DT, DT_AVG>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_AVG>, 1};
+        break;
+    default: break;
+    }
+    return k;
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bool vec,
+                          int device, cudaStream_t s)
+{
+    KernelInfo k;
+    if (dtype == DT_F32) k = pick_op<DT_F32>(op, p.P, vec);
+    else if (dtype == DT_BF16) k = pick_op<DT_BF16>(op, p.P, vec);
+    else if (dtype == DT_I32) k = pick_op<DT_I32>(op, p.P, vec);
+    if (!k.fn) return cudaErrorInvalidValue;
+
+    int resident = 0;
+    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(k.fn), kThreads, device, &resident);
+    if (e != cudaSuccess) return e;
+
+    const int epv = vec ? (dtype == DT_BF16 ? 8 : 4) : 1;
+    const uint64_t units = p.n / epv;
+    const uint64_t per_block = (uint64_t)kThreads * k.per_vec_iter;
+    uint64_t want = (units + per_block - 1) / per_block;
+    if (want < 1) want = 1;
+    uint64_t cap = resident / jobs;
+    if (cap < 1) cap = 1;
+    const unsigned gx = (unsigned)(want < cap ? want : cap);
+
+    count_launch();
+    k.fn<<<dim3(gx, (unsigned)jobs), kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dt

@@ -1,0 +1,247 @@
+"""Python binding of the dt C ABI (include/dt.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but turn Python arguments into C ones: tensors become their
+``data_ptr()``, lists become pointer arrays, a stream argument of ``None``
+becomes PyTorch's current stream on the group's device.  Every collective runs
+in the CUDA kernels of ``libdt.so``; there is no other code path.  Importing
+this module without the built library raises ``ImportError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdt.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "dt.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+        " (the collectives have no non-CUDA implementation)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_CUDA, DT_ERR_TIMEOUT, DT_ERR_OOM, \
+    DT_ERR_POISONED = range(7)
+DT_F32, DT_BF16, DT_I32 = 0, 1, 2
+DT_SUM, DT_AVG, DT_MAX, DT_MIN = 0, 1, 2, 3
+DT_MAX_RANKS = 16
+DT_ALL_RANKS = -1
+DT_SHARED_OUTPUT = 0x1
+DT_DEFAULT_BUCKET_CAP_BYTES = 25 << 20
+
+DTYPES = {"f32": DT_F32, "bf16": DT_BF16, "i32": DT_I32}
+OPS = {"sum": DT_SUM, "avg": DT_AVG, "max": DT_MAX, "min": DT_MIN}
+
+_vp = ctypes.c_void_p
+_vpp = ctypes.POINTER(ctypes.c_void_p)
+_sz = ctypes.c_size_t
+_szp = ctypes.POINTER(ctypes.c_size_t)
+_i = ctypes.c_int
+_u = ctypes.c_uint
+_u32 = ctypes.c_uint32
+
+_SIGS = {
+    "dt_group_create": ([_i, _i, ctypes.POINTER(_vp)], _i),
+    "dt_group_destroy": ([_vp], _i),
+    "dt_group_reset": ([_vp, _vp], _i),
+    "dt_group_check": ([_vp], _i),
+    "dt_group_error_detail": ([_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
+    "dt_group_size": ([_vp], _i),
+    "dt_group_generation": ([_vp], ctypes.c_int64),
+    "dt_group_set_timeout_ms": ([_vp, _u32], _i),
+    "dt_status_string": ([_i], ctypes.c_char_p),
+    "dt_launch_count": ([], ctypes.c_uint64),
+    "dt_allreduce": ([_vp, _i, _vpp, _vpp, _sz, _i, _i, _u, _vp], _i),
+    "dt_reduce_scatter": ([_vp, _i, _vpp, _vpp, _sz, _i, _i, _vp], _i),
+    "dt_all_gather": ([_vp, _i, _vpp, _vpp, _szp, _sz, _sz, _u, _vp], _i),
+    "dt_all_to_all": ([_vp, _i, _vpp, _vpp, _sz, _vp], _i),
+    "dt_bucket_allreduce": ([_vp, _vpp, _szp, _sz, _i, _i, _sz, _vp], _i),
+    "dt_bucket_plan": ([_szp, _sz, _sz, _sz, _szp, _szp], _i),
+    "dt_barrier": ([_vp, _i, _vp], _i),
+    "dt_debug_read_window": ([_vp, ctypes.POINTER(ctypes.c_int32), _vp], _i),
+    "dt_debug_ring_after_barrier": ([_vp, _vpp, _vpp, _vpp, _sz, _vp], _i),
+    "dt_debug_barrier_expect": ([_vp, _i, _u32, _vp], _i),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class DtError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {dt_status_string(status)} (status {status})")
+
+
+def header_symbols() -> list:
+    """Names of the functions include/dt.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(dt_\w+)\s*\(", text, re.M)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+# ------------------------------------------------------------ marshalling
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(xs: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * max(len(xs), 1))(*[_ptr(x) for x in xs])
+
+
+def _code(table: dict, v) -> int:
+    if isinstance(v, str):
+        return table[v]
+    try:
+        import torch
+        if isinstance(v, torch.dtype):
+            return {torch.float32: DT_F32, torch.bfloat16: DT_BF16, torch.int32: DT_I32}[v]
+    except ImportError:
+        pass
+    return int(v)
+
+
+def _stream(stream, device: int | None = None) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, what: str) -> None:
+    if st != DT_OK:
+        raise DtError(st, what)
+
+
+# ------------------------------------------------------------- functions
+def dt_status_string(status: int) -> str:
+    return _lib.dt_status_string(status).decode()
+
+
+def dt_launch_count() -> int:
+    return int(_lib.dt_launch_count())
+
+
+def dt_group_create(world_size: int, cuda_device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.dt_group_create(world_size, cuda_device, ctypes.byref(h)), "dt_group_create")
+    return h.value
+
+
+def dt_group_destroy(g: int) -> None:
+    _check(_lib.dt_group_destroy(g), "dt_group_destroy")
+
+
+def dt_group_reset(g: int, stream=None) -> None:
+    _check(_lib.dt_group_reset(g, _stream(stream)), "dt_group_reset")
+
+
+def dt_group_check(g: int) -> int:
+    """Returns the status code (does not raise)."""
+    return _lib.dt_group_check(g)
+
+
+def dt_group_error_detail(g: int):
+    r, p, gen = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = _lib.dt_group_error_detail(g, ctypes.byref(r), ctypes.byref(p), ctypes.byref(gen))
+    return code, r.value, p.value, gen.value
+
+
+def dt_group_size(g: int) -> int:
+    return _lib.dt_group_size(g)
+
+
+def dt_group_generation(g: int) -> int:
+    return int(_lib.dt_group_generation(g))
+
+
+def dt_group_set_timeout_ms(g: int, ms: int) -> None:
+    _check(_lib.dt_group_set_timeout_ms(g, ms), "dt_group_set_timeout_ms")
+
+
+def dt_allreduce(g: int, rank: int, ins: Sequence, outs: Sequence, count: int, dtype, op,
+                 flags: int = 0, stream=None) -> None:
+    _check(_lib.dt_allreduce(g, rank, _ptr_array(ins), _ptr_array(outs), count,
+                             _code(DTYPES, dtype), _code(OPS, op), flags, _stream(stream)),
+           "dt_allreduce")
+
+
+def dt_reduce_scatter(g: int, rank: int, ins: Sequence, outs: Sequence, recv_count: int, dtype,
+                      op, stream=None) -> None:
+    _check(_lib.dt_reduce_scatter(g, rank, _ptr_array(ins), _ptr_array(outs), recv_count,
+                                  _code(DTYPES, dtype), _code(OPS, op), _stream(stream)),
+           "dt_reduce_scatter")
+
+
+def dt_all_gather(g: int, rank: int, ins: Sequence, outs: Sequence, rows: Sequence | None,
+                  rows_equal: int, row_bytes: int, flags: int = 0, stream=None) -> None:
+    rows_arr = None if rows is None else (ctypes.c_size_t * max(len(rows), 1))(*rows)
+    _check(_lib.dt_all_gather(g, rank, _ptr_array(ins), _ptr_array(outs), rows_arr, rows_equal,
+                              row_bytes, flags, _stream(stream)), "dt_all_gather")
+
+
+def dt_all_to_all(g: int, rank: int, ins: Sequence, outs: Sequence, chunk_bytes: int,
+                  stream=None) -> None:
+    _check(_lib.dt_all_to_all(g, rank, _ptr_array(ins), _ptr_array(outs), chunk_bytes,
+                              _stream(stream)), "dt_all_to_all")
+
+
+def dt_bucket_allreduce(g: int, grads: Sequence[Sequence], counts: Sequence[int], dtype, op,
+                        bucket_cap_bytes: int = 0, stream=None) -> None:
+    """grads[t][p]: rank p's gradient t (tensor or device pointer)."""
+    flat = [x for row in grads for x in row]
+    cts = (ctypes.c_size_t * max(len(counts), 1))(*counts)
+    _check(_lib.dt_bucket_allreduce(g, _ptr_array(flat), cts, len(counts), _code(DTYPES, dtype),
+                                    _code(OPS, op), bucket_cap_bytes, _stream(stream)),
+           "dt_bucket_allreduce")
+
+
+def dt_bucket_plan(counts: Sequence[int], elem_bytes: int, cap_bytes: int):
+    T = len(counts)
+    cts = (ctypes.c_size_t * max(T, 1))(*counts)
+    out = (ctypes.c_size_t * max(T, 1))()
+    nb = ctypes.c_size_t()
+    _check(_lib.dt_bucket_plan(cts, T, elem_bytes, cap_bytes, out, ctypes.byref(nb)),
+           "dt_bucket_plan")
+    return [int(out[t]) for t in range(T)], int(nb.value)
+
+
+def dt_barrier(g: int, rank: int = DT_ALL_RANKS, stream=None) -> None:
+    _check(_lib.dt_barrier(g, rank, _stream(stream)), "dt_barrier")
+
+
+def dt_debug_read_window(g: int, stream=None):
+    import numpy as np
+    P = dt_group_size(g)
+    win = np.zeros((P, P), dtype=np.int32)
+    _check(_lib.dt_debug_read_window(g, win.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                     _stream(stream)), "dt_debug_read_window")
+    return win
+
+
+def dt_debug_ring_after_barrier(g: int, ins: Sequence, stage: Sequence, outs: Sequence,
+                                nbytes: int, stream=None) -> None:
+    _check(_lib.dt_debug_ring_after_barrier(g, _ptr_array(ins), _ptr_array(stage),
+                                            _ptr_array(outs), nbytes, _stream(stream)),
+           "dt_debug_ring_after_barrier")
+
+
+def dt_debug_barrier_expect(g: int, extra: int, timeout_ms: int, stream=None) -> None:
+    _check(_lib.dt_debug_barrier_expect(g, extra, timeout_ms, _stream(stream)),
+           "dt_debug_barrier_expect")

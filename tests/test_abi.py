@@ -1,0 +1,76 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/dt.h declares, and its host-only logic (argument checks that need no
+device, the bucket plan, status strings) behaves.  No compute call is made."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def dt():
+    import __graft_entry__
+    __graft_entry__.build()
+    from same_device_collective_gb300 import dt as mod
+    return mod
+
+
+def test_library_exports_every_header_symbol(dt):
+    names = dt.header_symbols()
+    assert len(names) >= 15
+    for name in ["dt_group_create", "dt_allreduce", "dt_reduce_scatter", "dt_all_gather",
+                 "dt_all_to_all", "dt_bucket_allreduce", "dt_barrier"]:
+        assert name in names
+    lib = dt.library()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_binding_has_the_c_names(dt):
+    for name in dt.header_symbols():
+        assert callable(getattr(dt, name)), name
+
+
+def test_status_strings(dt):
+    for code in range(7):
+        assert dt.dt_status_string(code)
+    assert dt.dt_status_string(99) == "unknown status"
+
+
+def test_null_group_is_invalid_without_touching_a_device(dt):
+    lib = dt.library()
+    assert lib.dt_allreduce(None, -1, None, None, 0, 0, 0, 0, None) == dt.DT_ERR_INVALID
+    assert lib.dt_reduce_scatter(None, -1, None, None, 0, 0, 0, None) == dt.DT_ERR_INVALID
+    assert lib.dt_all_gather(None, -1, None, None, None, 0, 0, 0, None) == dt.DT_ERR_INVALID
+    assert lib.dt_all_to_all(None, -1, None, None, 0, None) == dt.DT_ERR_INVALID
+    assert lib.dt_bucket_allreduce(None, None, None, 0, 0, 0, 0, None) == dt.DT_ERR_INVALID
+    assert lib.dt_barrier(None, -1, None) == dt.DT_ERR_INVALID
+    assert lib.dt_group_destroy(None) == dt.DT_ERR_INVALID
+    assert lib.dt_group_check(None) == dt.DT_ERR_INVALID
+    assert lib.dt_group_size(None) == 0
+    assert lib.dt_group_create(0, 0, None) == dt.DT_ERR_INVALID
+    h = ctypes.c_void_p()
+    assert lib.dt_group_create(17, 0, ctypes.byref(h)) == dt.DT_ERR_INVALID
+    assert lib.dt_group_create(0, 0, ctypes.byref(h)) == dt.DT_ERR_INVALID
+
+
+def test_bucket_plan_host_logic_matches_oracle(dt):
+    from same_device_collective_gb300 import workloads
+    rng = np.random.default_rng(5)
+    cases = [([10, 10, 10], 2, 40), ([30, 5, 30], 2, 40), ([], 2, 40), ([0, 100, 1], 2, 10),
+             (workloads.bucket_counts(), 2, workloads.BUCKET_CAP_BYTES),
+             ([int(c) for c in rng.integers(0, 5000, 500)], 4, 4096)]
+    for counts, es, cap in cases:
+        assert dt.dt_bucket_plan(counts, es, cap) == oracle.bucket_plan(counts, es, cap)
+    with pytest.raises(dt.DtError):
+        dt.dt_bucket_plan([1], 0, 10)
+    with pytest.raises(dt.DtError):
+        dt.dt_bucket_plan([1], 2, 0)
+
+
+def test_launch_counter_starts_at_zero_without_work(dt):
+    assert dt.dt_launch_count() >= 0
