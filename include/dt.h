@@ -62,7 +62,8 @@ typedef enum {
     DT_ERR_CUDA = 3,         /* a CUDA runtime call failed */
     DT_ERR_TIMEOUT = 4,      /* a device-side wait ran out of time (see dt_group_check) */
     DT_ERR_OOM = 5,          /* the group could not allocate its own state */
-    DT_ERR_POISONED = 6      /* an earlier timeout left the group unusable until reset */
+    DT_ERR_POISONED = 6,     /* an earlier timeout left the group unusable until reset */
+    DT_ERR_TOO_LARGE = 7     /* request exceeds the fixed scratch of dt_bucket_allreduce_static */
 } dt_status;
 
 typedef enum { DT_F32 = 0, DT_BF16 = 1, DT_I32 = 2 } dt_dtype;
@@ -188,6 +189,30 @@ dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_byt
  * win[r][r] == 0.  Each wait gives up after the group's time limit and
  * records DT_ERR_TIMEOUT. */
 dt_status dt_barrier(dt_group_t g, int rank, void *stream);
+
+/* Allocation-free fused bucket all-reduce.  The pages have no counterpart:
+ * this entry point exists for callers that cannot let a library allocate
+ * device memory -- applications that own all device memory through their own
+ * pool (cudaMalloc synchronises the device and escapes their accounting) and
+ * code running while a global-mode stream capture is active, where cudaMalloc
+ * is not permitted.  Such callers cannot create a dt_group.
+ *   world_size        P (1..DT_MAX_RANKS); no group is needed
+ *   grads, counts, n_tensors, dtype, op, bucket_cap_bytes, stream
+ *                     as dt_bucket_allreduce; the results are identical
+ * The chunk and pointer tables live in one fixed 1 MiB device array inside
+ * this library (every GPU that loads the library holds it until the process
+ * exits) and are staged from a fixed host array: the call allocates nothing.
+ * Tables that do not fit (n_tensors * P * 8 bytes of pointers plus 16 bytes
+ * per 32768-element chunk) return DT_ERR_TOO_LARGE before anything is
+ * enqueued.  Every call shares the array and leaves its contents behind;
+ * calls that overlap on the GPU (unordered streams) race on it, calls on one
+ * stream do not.  No signal barrier runs between buckets (there is no group
+ * window); stream order orders them.  The first call on each device looks up
+ * the array's device address with that device current: make it before any
+ * stream capture begins.  The current CUDA device must be the gradients'. */
+dt_status dt_bucket_allreduce_static(int world_size, void *const *grads, const size_t *counts,
+                                     size_t n_tensors, int dtype, int op,
+                                     size_t bucket_cap_bytes, void *stream);
 
 /* ------------------------------------------------------------- test hooks */
 

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "dt")
 LIB = os.path.join(PKG, "libdt.so")
 
-SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu"]
+SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu",
+           "dt_static.cu"]
 HEADERS = ["dt_internal.h", "dt_math.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -215,6 +215,7 @@ const char *dt_status_string(dt_status st)
     case DT_ERR_TIMEOUT: return "device wait timed out";
     case DT_ERR_OOM: return "out of memory";
     case DT_ERR_POISONED: return "group poisoned by an earlier device error; reset it";
+    case DT_ERR_TOO_LARGE: return "request exceeds the fixed scratch of the allocation-free entry point";
     }
     return "unknown status";
 }

@@ -1,0 +1,150 @@
+// Allocation-free variant of the fused bucket all-reduce.
+//
+// Some callers cannot let a library call cudaMalloc: applications that own
+// all device memory through their own pool (cudaMalloc synchronises the
+// device and bypasses their accounting), and code that runs while a stream
+// capture in global mode is active, where cudaMalloc is not permitted.  They
+// cannot create a dt_group, which allocates its window and plan scratch.
+// dt_bucket_allreduce_static serves them: the chunk and pointer tables that
+// the bucket kernel reads live in a fixed file-scope device array of
+// kStaticScratchBytes, staged from a fixed host array, so a call allocates
+// nothing on the device or the host.
+//
+// Costs and rules of the fixed array:
+//   - every GPU that loads this library holds the array (1 MiB) until the
+//     process exits;
+//   - every call shares it and it keeps the last call's contents; each call
+//     overwrites the part it uses before its kernels read it;
+//   - calls that overlap on the GPU (issued on different streams without
+//     ordering between them) race on the array; calls on one stream are safe;
+//   - the first call on each device looks up the array's device address
+//     (cudaGetSymbolAddress) with that device current; make that first call
+//     before any stream capture begins.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "dt_internal.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)1 << 20;
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_bucket_scratch[kStaticScratchBytes];
+
+// Host staging of the same size: copied with a pageable cudaMemcpyAsync,
+// which returns once the bytes have left this array.
+alignas(256) unsigned char h_bucket_staging[kStaticScratchBytes];
+std::mutex g_static_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Set-up, once per device, with that device current.
+cudaError_t scratch_address(int device, void **out)
+{
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_scratch_addr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_bucket_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[device] = p;
+    }
+    *out = g_scratch_addr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *grads,
+                                                const size_t *counts, size_t n_tensors, int dtype,
+                                                int op, size_t bucket_cap_bytes, void *stream)
+{
+    if (world_size < 1 || world_size > DT_MAX_RANKS) return DT_ERR_INVALID;
+    if (dtype != DT_BF16 && dtype != DT_F32)
+        return dtype == DT_I32 ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
+    if (op != DT_SUM && op != DT_AVG)
+        return (op == DT_MAX || op == DT_MIN) ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
+    if (n_tensors && (!grads || !counts)) return DT_ERR_INVALID;
+    const int P = world_size;
+    const size_t es = dtype == DT_BF16 ? 2 : 4;
+    const size_t cap = bucket_cap_bytes ? bucket_cap_bytes : DT_DEFAULT_BUCKET_CAP_BYTES;
+
+    // size check first: the tables must fit the fixed array
+    if (n_tensors > kStaticScratchBytes / (sizeof(void *) * P)) return DT_ERR_TOO_LARGE;
+    size_t nchunks = 0;
+    for (size_t t = 0; t < n_tensors; ++t) {
+        if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
+        nchunks += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
+        for (int p = 0; p < P && counts[t]; ++p)
+            if (!grads[t * P + p]) return DT_ERR_INVALID;
+    }
+    const size_t ptr_bytes = n_tensors * P * sizeof(void *);
+    if (nchunks > (kStaticScratchBytes - ptr_bytes) / sizeof(dt::BucketChunk)) return DT_ERR_TOO_LARGE;
+    if (nchunks == 0) return DT_OK;
+
+    // no two gradient buffers may overlap: quadratic check, no allocation
+    for (size_t t = 0; t < n_tensors; ++t)
+        for (int p = 0; p < P && counts[t]; ++p) {
+            const uintptr_t lo = (uintptr_t)grads[t * P + p], hi = lo + counts[t] * es;
+            for (size_t u = t; u < n_tensors; ++u)
+                for (int q = (u == t ? p + 1 : 0); q < P && counts[u]; ++q) {
+                    const uintptr_t lo2 = (uintptr_t)grads[u * P + q], hi2 = lo2 + counts[u] * es;
+                    if (lo < hi2 && lo2 < hi) return DT_ERR_INVALID;
+                }
+        }
+
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return DT_ERR_CUDA;
+    void *scratch = nullptr;
+    if (scratch_address(device, &scratch) != cudaSuccess) return DT_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // plan: [T * P pointers][chunks in tensor order]; buckets are consecutive
+    // tensors, greedy in order under the cap, as in dt_bucket_plan
+    memcpy(h_bucket_staging, grads, ptr_bytes);
+    dt::BucketChunk *chunks = reinterpret_cast<dt::BucketChunk *>(h_bucket_staging + ptr_bytes);
+    size_t c = 0;
+    for (size_t t = 0; t < n_tensors; ++t) {
+        bool al = true;
+        for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
+        for (size_t beg = 0; beg < counts[t]; beg += dt::kBucketChunkElems) {
+            chunks[c].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
+            chunks[c].nelem = (uint32_t)std::min<size_t>(dt::kBucketChunkElems, counts[t] - beg);
+            chunks[c].begin = beg;
+            ++c;
+        }
+    }
+    cudaError_t e = cudaMemcpyAsync(scratch, h_bucket_staging, ptr_bytes + c * sizeof(dt::BucketChunk),
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return DT_ERR_CUDA;
+
+    const unsigned char *d = static_cast<const unsigned char *>(scratch);
+    dt::BucketParams bp;
+    bp.ptrs = reinterpret_cast<void *const *>(d);
+    bp.P = P;
+    bp.avg_pow2 = (P & (P - 1)) == 0;
+    bp.avg_scale = bp.avg_pow2 ? 1.0f / (float)P : 0.0f;
+    // one launch per bucket, no signal barrier between buckets: with no group
+    // there is no window, and stream order already orders the buckets
+    size_t first = 0, filled = 0;
+    c = 0;
+    for (size_t t = 0; t <= n_tensors; ++t) {
+        const bool close = t == n_tensors ||
+                           (filled > 0 && filled + counts[t] * es > cap);
+        if (close && c > first) {
+            bp.chunks = reinterpret_cast<const dt::BucketChunk *>(d + ptr_bytes) + first;
+            bp.nchunks = (uint32_t)(c - first);
+            e = dt::launch_bucket(bp, dtype, op, device, s);
+            if (e != cudaSuccess) return DT_ERR_CUDA;
+            first = c;
+        }
+        if (close) filled = 0;
+        if (t == n_tensors) break;
+        filled += counts[t] * es;
+        c += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
+    }
+    return DT_OK;
+}

@@ -26,7 +26,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_CUDA, DT_ERR_TIMEOUT, DT_ERR_OOM, \
-    DT_ERR_POISONED = range(7)
+    DT_ERR_POISONED, DT_ERR_TOO_LARGE = range(8)
 DT_F32, DT_BF16, DT_I32 = 0, 1, 2
 DT_SUM, DT_AVG, DT_MAX, DT_MIN = 0, 1, 2, 3
 DT_MAX_RANKS = 16
@@ -62,6 +62,7 @@ _SIGS = {
     "dt_all_to_all": ([_vp, _i, _vpp, _vpp, _sz, _vp], _i),
     "dt_bucket_allreduce": ([_vp, _vpp, _szp, _sz, _i, _i, _sz, _vp], _i),
     "dt_bucket_plan": ([_szp, _sz, _sz, _sz, _szp, _szp], _i),
+    "dt_bucket_allreduce_static": ([_i, _vpp, _szp, _sz, _i, _i, _sz, _vp], _i),
     "dt_barrier": ([_vp, _i, _vp], _i),
     "dt_debug_read_window": ([_vp, ctypes.POINTER(ctypes.c_int32), _vp], _i),
     "dt_debug_ring_after_barrier": ([_vp, _vpp, _vpp, _vpp, _sz, _vp], _i),
@@ -210,6 +211,17 @@ def dt_bucket_allreduce(g: int, grads: Sequence[Sequence], counts: Sequence[int]
     _check(_lib.dt_bucket_allreduce(g, _ptr_array(flat), cts, len(counts), _code(DTYPES, dtype),
                                     _code(OPS, op), bucket_cap_bytes, _stream(stream)),
            "dt_bucket_allreduce")
+
+
+def dt_bucket_allreduce_static(world_size: int, grads: Sequence[Sequence], counts: Sequence[int],
+                               dtype, op, bucket_cap_bytes: int = 0, stream=None) -> None:
+    """Allocation-free bucket all-reduce: no group, tables in the library's
+    fixed device array (see include/dt.h).  grads[t][p] as dt_bucket_allreduce."""
+    flat = [x for row in grads for x in row]
+    cts = (ctypes.c_size_t * max(len(counts), 1))(*counts)
+    _check(_lib.dt_bucket_allreduce_static(world_size, _ptr_array(flat), cts, len(counts),
+                                           _code(DTYPES, dtype), _code(OPS, op), bucket_cap_bytes,
+                                           _stream(stream)), "dt_bucket_allreduce_static")
 
 
 def dt_bucket_plan(counts: Sequence[int], elem_bytes: int, cap_bytes: int):

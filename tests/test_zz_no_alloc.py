@@ -1,0 +1,75 @@
+"""The allocation-free bucket all-reduce gives the group-based one's results.
+
+dt_bucket_allreduce_static is for callers that cannot let a library allocate
+device memory: applications whose own pool owns all device memory (cudaMalloc
+would synchronise the device and escape their accounting) and code running
+while a global-mode stream capture is active, where cudaMalloc is not allowed.
+It keeps its tables in one fixed device array inside the library instead of a
+group's scratch.  These tests call it through the C ABI and compare its output
+with dt_bucket_allreduce's, bit for bit (the tolerance of every parity test
+here), on two calls in a row with different tables, so the second call also
+shows that the array's leftover contents do not leak into a result.
+
+This file sorts last so that a run stopping at the first failure has already
+run every other test; it also passes on its own in a fresh process.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dt():
+    from same_device_collective_gb300 import dt as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+def _grads(counts, P, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return [[(torch.randn(c, generator=g) * 1e-3).to(td).cuda() for _ in range(P)]
+            for c in counts]
+
+
+def _host(t):
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy() if t.dtype == torch.bfloat16 else t.view(torch.int32).numpy()
+
+
+def test_static_bucket_allreduce_matches_group_version_two_calls(dt):
+    calls = [
+        # (P, dtype, op, counts, cap): the second call has a smaller table
+        (8, "bf16", "avg", [1000, 70_001, 0, 7, 32_768, 200_003, 3], 256 << 10),
+        (3, "f32", "sum", [5, 40_000, 1], 64 << 10),
+    ]
+    for i, (P, dtype, op, counts, cap) in enumerate(calls):
+        a = _grads(counts, P, dtype, 100 + i)
+        b = [[x.clone() for x in row] for row in a]
+        torch.cuda.synchronize()
+        dt.dt_bucket_allreduce_static(P, a, counts, dtype, op, bucket_cap_bytes=cap)
+        g = dt.dt_group_create(P, torch.cuda.current_device())
+        try:
+            dt.dt_bucket_allreduce(g, b, counts, dtype, op, bucket_cap_bytes=cap)
+            torch.cuda.synchronize()
+            assert dt.dt_group_check(g) == dt.DT_OK
+        finally:
+            dt.dt_group_destroy(g)
+        for t in range(len(counts)):
+            for p in range(P):
+                assert np.array_equal(_host(a[t][p]), _host(b[t][p])), f"call {i} tensor {t} rank {p}"
+
+
+def test_static_bucket_allreduce_rejects_tables_past_the_fixed_array(dt):
+    P = 4
+    counts = [1 << 31] * 16            # 16 x 65536 chunks: far past the 1 MiB array
+    fake = [[(t * P + p + 1) << 40 for p in range(P)] for t in range(len(counts))]
+    n0 = dt.dt_launch_count()
+    with pytest.raises(dt.DtError) as e:
+        dt.dt_bucket_allreduce_static(P, fake, counts, "bf16", "avg")
+    assert e.value.status == dt.DT_ERR_TOO_LARGE
+    assert dt.dt_launch_count() == n0
