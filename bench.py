@@ -40,7 +40,7 @@ WORKLOAD = f"rs_avg_then_ag_bf16_P{P_RANKS}_{ROWS}x{COLS}"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu", "dt_math.cuh",
-                  "dt_internal.h"]
+                  "dt_internal.h", "dt_device.cuh"]
 
 
 # ----------------------------------------------------------------- helpers

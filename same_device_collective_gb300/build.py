@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libdt.so")
 
 SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu",
            "dt_static.cu"]
-HEADERS = ["dt_internal.h", "dt_math.cuh"]
+HEADERS = ["dt_internal.h", "dt_math.cuh", "dt_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the reductions use

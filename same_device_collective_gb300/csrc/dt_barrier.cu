@@ -19,6 +19,7 @@
 // a rank that gives up records DT_ERR_TIMEOUT once in the error word and its
 // host-mapped mirror and returns, so the GPU is never held.
 #include "dt_internal.h"
+#include "dt_device.cuh"
 
 namespace dt {
 namespace {
@@ -35,30 +36,12 @@ __device__ __forceinline__ int32_t load_acquire(const int32_t *cell)
     return v;
 }
 
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ void record_error(const BarrierParams &p, int code, int rank, int peer, int gen)
-{
-    if (atomicCAS(&p.err->code, 0, code) == 0) {
-        p.err->rank = rank;
-        p.err->peer = peer;
-        p.err->gen = gen;
-        volatile DevError *h = p.err_host;
-        h->rank = rank;
-        h->peer = peer;
-        h->gen = gen;
-        __threadfence_system();
-        h->code = code;
-        __threadfence_system();
-    }
-}
-
-// Run by the 32 lanes of one warp for rank r; true when every wait ended in time.
+// Run by the 32 lanes of one warp for rank r; true when every wait ended in
+// time.  kFence orders writes made earlier in the same kernel (by any thread
+// of the block, after a __syncthreads) before the notifies, and the peers'
+// writes before the block's later reads; the stand-alone barrier kernel has
+// no such writes (everything before it finished in stream order) and skips it.
+template <bool kFence>
 __device__ bool rank_barrier(const BarrierParams &p, int r)
 {
     const int lane = threadIdx.x & 31;
@@ -66,29 +49,29 @@ __device__ bool rank_barrier(const BarrierParams &p, int r)
     const int32_t g = p.rank_gen[r] + 1;
     const bool peer = lane < P && lane != r;
 
-    __threadfence();                     // this rank's earlier writes before its notifies
+    if (kFence) __threadfence();         // this rank's earlier writes before its notifies
     if (peer) notify_add(&p.win[lane * P + r]);
 
     bool ok = true;
     if (peer) {
         const int32_t want = g + p.extra;
         const uint64_t t0 = global_ns();
-        const uint64_t max_polls = p.timeout_ns / 256 + 4096;
+        const uint64_t max_polls = p.sink.timeout_ns / 256 + 4096;
         uint32_t sleep_ns = 0;
         for (uint64_t it = 0;; ++it) {
             const int32_t v = load_acquire(&p.win[r * P + lane]);
             if ((int32_t)(v - want) >= 0) break;          // Ge, safe across wrap-around
-            if (it >= max_polls || global_ns() - t0 > p.timeout_ns) { ok = false; break; }
+            if (it >= max_polls || global_ns() - t0 > p.sink.timeout_ns) { ok = false; break; }
             if (it >= 64) {
                 sleep_ns = sleep_ns ? (sleep_ns < 256 ? sleep_ns * 2 : 256) : 32;
                 __nanosleep(sleep_ns);
             }
         }
     }
-    __threadfence();                     // peers' writes before this rank's later reads
+    if (kFence) __threadfence();         // peers' writes before this rank's later reads
     const unsigned bad = __ballot_sync(0xFFFFFFFFu, !ok);
     if (lane == 0) {
-        if (bad) record_error(p, DT_ERR_TIMEOUT, r, __ffs(bad) - 1, g);
+        if (bad) record_error(p.sink, DT_ERR_TIMEOUT, r, __ffs(bad) - 1, g);
         p.rank_gen[r] = g;
     }
     __syncwarp();
@@ -97,7 +80,8 @@ __device__ bool rank_barrier(const BarrierParams &p, int r)
 
 __global__ void __launch_bounds__(32) barrier_kernel(const __grid_constant__ BarrierParams p)
 {
-    rank_barrier(p, blockIdx.x);
+    pdl_begin();
+    rank_barrier<false>(p, blockIdx.x);
 }
 
 __device__ void copy_bytes(unsigned char *dst, const unsigned char *src, uint64_t n)
@@ -117,10 +101,11 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ 
 {
     __shared__ int ok;
     const int r = blockIdx.x;
+    pdl_begin();
     copy_bytes(p.stage[r], p.in[r], p.bytes);
     __syncthreads();
     if (threadIdx.x < 32) {
-        const bool passed = rank_barrier(p.bar, r);
+        const bool passed = rank_barrier<true>(p.bar, r);
         if (threadIdx.x == 0) ok = passed;
     }
     __syncthreads();
@@ -131,18 +116,12 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ 
 
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s)
 {
-    void *args[] = {const_cast<BarrierParams *>(&p)};
-    count_launch();
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(barrier_kernel),
-                                       dim3(p.P), dim3(32), args, 0, s);
+    return launch_kernel(barrier_kernel, dim3(p.P), dim3(32), 0, s, true, p);
 }
 
 cudaError_t launch_ring(const RingParams &p, cudaStream_t s)
 {
-    void *args[] = {const_cast<RingParams *>(&p)};
-    count_launch();
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel),
-                                       dim3(p.bar.P), dim3(kThreads), args, 0, s);
+    return launch_kernel(ring_kernel, dim3(p.bar.P), dim3(kThreads), 0, s, true, p);
 }
 
 }  // namespace dt

@@ -10,14 +10,15 @@
 // each block reduces its chunks in place in every rank's gradient, reading
 // each element once per rank and writing it once per rank.
 #include "dt_internal.h"
+#include "dt_device.cuh"
 #include "dt_math.cuh"
 
 namespace dt {
 namespace {
 
 template <int PMAX>
-struct BucketUnroll {   // 16 loads of 16 bytes in flight per thread
-    static constexpr int U = PMAX >= 16 ? 1 : 16 / PMAX;
+struct BucketUnroll {   // 8 loads of 16 bytes in flight per thread (16 at P > 8)
+    static constexpr int U = PMAX >= 8 ? 1 : 8 / PMAX;
 };
 
 template <int DT, int OP, int PMAX>
@@ -28,6 +29,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;
     __shared__ void *sp[DT_MAX_RANKS];
     const int P = p.P;
+    pdl_begin();
 
     for (uint32_t c = blockIdx.x; c < p.nchunks; c += gridDim.x) {
         const BucketChunk ch = p.chunks[c];
@@ -51,7 +53,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                     if (v < nvec) {
 #pragma unroll
                         for (int r = 0; r < PMAX; ++r)
-                            if (r < P) x[u][r] = __ldcg(in[r] + v);
+                            if (r < P) x[u][r] = __ldcs(in[r] + v);
                     }
                 }
 #pragma unroll
@@ -61,7 +63,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                         const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
 #pragma unroll
                         for (int r = 0; r < PMAX; ++r)
-                            if (r < P) __stcg(static_cast<uint4 *>(sp[r]) + v0 + v, y);
+                            if (r < P) __stcs(static_cast<uint4 *>(sp[r]) + v0 + v, y);
                     }
                 }
             }
@@ -98,9 +100,7 @@ cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, 
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
     if (e != cudaSuccess) return e;
     const unsigned gx = p.nchunks < (uint32_t)resident ? p.nchunks : (unsigned)resident;
-    count_launch();
-    fn<<<gx, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3(gx), dim3(kThreads), 0, s, false, p);
 }
 
 }  // namespace dt

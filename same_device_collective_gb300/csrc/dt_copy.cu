@@ -1,21 +1,25 @@
-// Byte-copy kernel behind AllGather (equal and uneven shards) and AllToAll.
+// Byte-copy kernels behind AllGather (equal and uneven shards) and AllToAll.
 //
 // Both collectives of the DTorch ThreadGroup interface (§2.1) are pure data
 // movement: AllGather writes every rank's shard into every rank's output at
 // the shard's row offset, AllToAll sends chunk j of rank i to rank j.  The
 // host turns a call into a list of segments (source range -> one or more
-// destinations at one offset); this kernel moves them in one launch.  Each
-// segment is cut into 16 KiB tiles; a resident grid strides over the tiles
-// of all segments.  A block loads its tile once into registers (four 16-byte
-// vectors per thread, all in flight together) and stores it to every
-// destination of the segment, so a shard is read from HBM once however many
-// ranks receive it.
+// destinations at one offset); one launch moves them all.  Each segment is
+// cut into tiles and a resident grid strides over the tiles of all segments.
+//
+// 16-byte-aligned segments go through the copy engine (TMA bulk copies): a
+// tile is loaded from HBM into shared memory once and stored from there to
+// every destination of its segment, so a shard is read once however many
+// ranks receive it and no register or load/store-unit traffic is spent on the
+// bytes.  Destinations are written once and not read back here, so the
+// stores carry an evict-first L2 policy: their dirty lines leave L2 early
+// instead of being written back during the next kernel.  Anything else takes
+// a byte-wise kernel with the same tiling.
 #include "dt_internal.h"
+#include "dt_device.cuh"
 
 namespace dt {
 namespace {
-
-constexpr int kVecPerThread = kCopyTileBytes / (16 * kThreads);   // 4
 
 template <int NSEG>
 __device__ __forceinline__ int find_seg(const CopyParams<NSEG> &p, uint64_t tile)
@@ -29,31 +33,76 @@ __device__ __forceinline__ int find_seg(const CopyParams<NSEG> &p, uint64_t tile
     return lo;
 }
 
+// Bulk-copy (TMA) kernel for 16-byte-aligned segments.  One thread per block
+// drives the copy engine: it keeps kBulkStages tiles of
+// shared memory in flight (global -> shared bulk loads that complete on one
+// mbarrier per stage) and, as each tile lands, issues one shared -> global
+// bulk store per destination of its segment.  A stage is refilled once the
+// stores of the tile it held have finished reading it (bulk async-groups).
+// Every mbarrier wait is bounded: a wait that runs out records DT_ERR_TIMEOUT
+// (rank -1, peer = tile), drains the loads still in flight with bounded waits
+// and returns.
+constexpr int kBulkStages = 6;
+constexpr int kBulkTile = 32768;
+constexpr int kBulkThreads = 32;
+constexpr size_t kBulkSmem = 128 + (size_t)kBulkStages * kBulkTile;
+
 template <int NSEG>
-__global__ void __launch_bounds__(kThreads)
-copy_vec_kernel(const __grid_constant__ CopyParams<NSEG> p)
+__global__ void __launch_bounds__(kBulkThreads)
+copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG> p)
 {
-    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    pdl_begin();
+    if (threadIdx.x != 0) return;
+    const uint64_t first = blockIdx.x, step = gridDim.x;
+    if (first >= p.total_tiles) return;
+    const uint64_t n = (p.total_tiles - first + step - 1) / step;   // tiles of this block
+    const uint32_t bar0 = smem_addr(smem);
+    const uint32_t buf0 = smem_addr(smem + 128);
+    for (int k = 0; k < kBulkStages; ++k) mbar_init(bar0 + 8 * k, 1);
+    mbar_init_fence();
+    const uint64_t pol = policy_evict_first();
+
+    auto issue_load = [&](uint64_t i) {
+        const uint64_t tile = first + i * step;
         const CopySeg &sg = p.seg[find_seg(p, tile)];
-        const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;   // byte offset in segment
-        const uint64_t nv = (sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes) / 16;
-        const uint4 *src = reinterpret_cast<const uint4 *>(sg.src + t0);
-        uint4 x[kVecPerThread];
-#pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
-            const uint64_t v = (uint64_t)u * kThreads + threadIdx.x;
-            if (v < nv) x[u] = __ldcg(src + v);
+        const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
+        const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
+        const int k = (int)(i % kBulkStages);
+        mbar_expect_tx(bar0 + 8 * k, nb);
+        bulk_load(buf0 + k * kBulkTile, sg.src + t0, nb, bar0 + 8 * k);
+    };
+
+    const uint64_t pre = n < (uint64_t)kBulkStages ? n : (uint64_t)kBulkStages;
+    for (uint64_t i = 0; i < pre; ++i) issue_load(i);
+    uint64_t issued = pre;
+
+    for (uint64_t i = 0; i < n; ++i) {
+        const int k = (int)(i % kBulkStages);
+        if (!mbar_wait_bounded(bar0 + 8 * k, (uint32_t)((i / kBulkStages) & 1), p.sink.timeout_ns)) {
+            record_error(p.sink, DT_ERR_TIMEOUT, -1, (int)(first + i * step), 0);
+            for (uint64_t j = i + 1; j < issued; ++j)   // let the other loads land (bounded)
+                mbar_wait_bounded(bar0 + 8 * (int)(j % kBulkStages),
+                                  (uint32_t)((j / kBulkStages) & 1), p.sink.timeout_ns);
+            break;
         }
-        for (int k = 0; k < sg.dst_count; ++k) {
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                static_cast<unsigned char *>(p.out[sg.dst_first + k]) + sg.dst_off + t0);
-#pragma unroll
-            for (int u = 0; u < kVecPerThread; ++u) {
-                const uint64_t v = (uint64_t)u * kThreads + threadIdx.x;
-                if (v < nv) __stcg(dst + v, x[u]);
-            }
+        fence_async_shared();
+        const uint64_t tile = first + i * step;
+        const CopySeg &sg = p.seg[find_seg(p, tile)];
+        const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
+        const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
+        for (int d = 0; d < sg.dst_count; ++d)
+            bulk_store_hint(static_cast<unsigned char *>(p.out[sg.dst_first + d]) + sg.dst_off + t0,
+                            buf0 + k * kBulkTile, nb, pol);
+        bulk_commit();
+        // refill the stage of tile i-1 once its stores have read it
+        if (i >= 1 && issued < n) {
+            bulk_wait_read<1>();
+            issue_load(issued);
+            ++issued;
         }
     }
+    bulk_wait_all();
 }
 
 // Any alignment: byte by byte, same tiling.
@@ -61,6 +110,7 @@ template <int NSEG>
 __global__ void __launch_bounds__(kThreads)
 copy_byte_kernel(const __grid_constant__ CopyParams<NSEG> p)
 {
+    pdl_begin();
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         const CopySeg &sg = p.seg[find_seg(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
@@ -74,13 +124,14 @@ copy_byte_kernel(const __grid_constant__ CopyParams<NSEG> p)
 }
 
 template <int NSEG>
-cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec, int device,
-                     cudaStream_t s)
+cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec,
+                     const ErrorSink &sink, int device, cudaStream_t s)
 {
     CopyParams<NSEG> p;
     memset(&p, 0, sizeof p);
     for (int r = 0; r < DT_MAX_RANKS; ++r) p.out[r] = out[r];
-    p.tile_bytes = vec ? kCopyTileBytes : 4096;
+    p.sink = sink;
+    p.tile_bytes = vec ? (uint64_t)kBulkTile : 4096;
     uint64_t tiles = 0;
     int used = 0;
     for (int i = 0; i < nseg; ++i) {
@@ -94,23 +145,38 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec, 
     p.nseg = used;
     p.total_tiles = tiles;
 
-    void (*fn)(CopyParams<NSEG>) = vec ? copy_vec_kernel<NSEG> : copy_byte_kernel<NSEG>;
+    if (vec) {
+        void (*fn)(CopyParams<NSEG>) = copy_bulk_kernel<NSEG>;
+        static bool attr_set = false;   // per instantiation; the attribute is per function
+        if (!attr_set) {
+            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kBulkSmem);
+            if (e != cudaSuccess) return e;
+            attr_set = true;
+        }
+        int resident = 0;
+        cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
+                                        &resident, kBulkSmem);
+        if (e != cudaSuccess) return e;
+        const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
+        return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), kBulkSmem, s, false, p);
+    }
+    void (*fn)(CopyParams<NSEG>) = copy_byte_kernel<NSEG>;
     int resident = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
     if (e != cudaSuccess) return e;
     const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
-    count_launch();
-    fn<<<(unsigned)gx, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
 }
 
 }  // namespace
 
-cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec, int device,
-                        cudaStream_t s)
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec,
+                        const ErrorSink &sink, int device, cudaStream_t s)
 {
-    if (nseg <= DT_MAX_RANKS) return launch_n<DT_MAX_RANKS>(segs, nseg, out, vec, device, s);
-    if (nseg <= kMaxSeg) return launch_n<kMaxSeg>(segs, nseg, out, vec, device, s);
+    if (nseg <= DT_MAX_RANKS) return launch_n<DT_MAX_RANKS>(segs, nseg, out, vec, sink, device, s);
+    if (nseg <= kMaxSeg) return launch_n<kMaxSeg>(segs, nseg, out, vec, sink, device, s);
     return cudaErrorInvalidValue;
 }
 

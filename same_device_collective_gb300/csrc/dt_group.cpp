@@ -26,6 +26,15 @@ static std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char *env = std::getenv("DT_PDL");
+        return !(env && env[0] == '0');
+    }();
+    return on;
+}
+
 int sm_count(int device)
 {
     static std::mutex mu;
@@ -40,18 +49,19 @@ int sm_count(int device)
     return n;
 }
 
-cudaError_t resident_blocks(const void *fn, int threads, int device, int *out)
+cudaError_t resident_blocks(const void *fn, int threads, int device, int *out, size_t dyn_smem)
 {
     static std::mutex mu;
     static std::unordered_map<uint64_t, int> cache;
-    const uint64_t key = reinterpret_cast<uintptr_t>(fn) * 131u + (uint64_t)device * 7u + threads;
+    const uint64_t key = reinterpret_cast<uintptr_t>(fn) * 131u + (uint64_t)device * 7u + threads +
+                         (uint64_t)dyn_smem * 1000003u;
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
         if (it != cache.end()) { *out = it->second; return cudaSuccess; }
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, dyn_smem);
     if (e != cudaSuccess) return e;
     const int n = sm_count(device) * (per_sm > 0 ? per_sm : 1);
     std::lock_guard<std::mutex> lock(mu);
@@ -135,15 +145,15 @@ dt::BarrierParams barrier_params(dt_group *g, int extra, uint64_t timeout_ns)
     dt::BarrierParams b;
     b.win = g->d_win;
     b.rank_gen = g->d_win + (size_t)g->P * g->P;
-    b.err = g->d_err;
-    b.err_host = g->h_err_dev;
-    b.timeout_ns = timeout_ns;
+    b.sink = dt::ErrorSink{g->d_err, g->h_err_dev, timeout_ns};
     b.P = g->P;
     b.extra = extra;
     return b;
 }
 
 uint64_t timeout_ns(const dt_group *g) { return (uint64_t)g->timeout_ms * 1000000ull; }
+
+dt::ErrorSink error_sink(dt_group *g) { return dt::ErrorSink{g->d_err, g->h_err_dev, timeout_ns(g)}; }
 
 dt_status issue_barrier(dt_group *g, cudaStream_t s)
 {
@@ -506,7 +516,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
     }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs, P, outs, vec, g->device,
+    return cuda_status(dt::launch_copy(segs, P, outs, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -557,7 +567,7 @@ dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *con
     for (int q = 0; q < P; ++q) outs[q] = out[q];
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, vec, g->device,
+    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 

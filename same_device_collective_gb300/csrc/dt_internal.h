@@ -8,6 +8,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "dt.h"
 
@@ -15,7 +16,6 @@ namespace dt {
 
 constexpr int kThreads = 256;                          // threads per block, all data kernels
 constexpr int kMaxSeg = DT_MAX_RANKS * DT_MAX_RANKS;   // all-to-all: P^2 chunk copies
-constexpr int kCopyTileBytes = 16384;                  // one block moves 16 KiB per tile
 constexpr uint32_t kBucketChunkElems = 32768;          // bucket work unit, elements
 
 // First device-side failure, written once (atomicCAS on code) by the kernel
@@ -26,6 +26,13 @@ struct DevError {
     int32_t rank;
     int32_t peer;
     int32_t gen;
+};
+
+// Where a kernel with a bounded wait reports that the wait ran out.
+struct ErrorSink {
+    DevError *err;        // device error word
+    DevError *err_host;   // device view of its host-mapped mirror
+    uint64_t timeout_ns;
 };
 
 // ---- reduction (AllReduce, ReduceScatter) ---------------------------------
@@ -60,6 +67,7 @@ struct CopySeg {
 template <int NSEG>
 struct CopyParams {
     void *out[DT_MAX_RANKS];
+    ErrorSink sink;
     uint64_t tile_bytes;
     uint64_t total_tiles;
     int32_t nseg;
@@ -90,9 +98,7 @@ struct BucketParams {
 struct BarrierParams {
     int32_t *win;        // [P][P]
     int32_t *rank_gen;   // [P]: barriers rank r has passed
-    DevError *err;       // device error word
-    DevError *err_host;  // device view of the host-mapped mirror
-    uint64_t timeout_ns;
+    ErrorSink sink;
     int32_t P;
     int32_t extra;       // added to the threshold (failure injection); 0 normally
 };
@@ -107,14 +113,48 @@ struct RingParams {
 
 // ---- launchers (one per kernel family; each counts its launches) ----------
 void count_launch();
+
+// Programmatic dependent launch: kernels launched with it may start while the
+// previous kernel on the stream finishes; every kernel here waits on its
+// prerequisite grid (griddepcontrol.wait) before touching memory.  On by
+// default; the environment variable DT_PDL=0 turns it off.
+bool pdl_enabled();
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool cooperative, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    unsigned n = 0;
+    if (pdl_enabled()) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cooperative) {
+        attrs[n].id = cudaLaunchAttributeCooperative;
+        attrs[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    count_launch();
+    return cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
+}
 int sm_count(int device);
 // SMs x blocks of `fn` one SM holds at once (cached per kernel and device).
-cudaError_t resident_blocks(const void *fn, int threads, int device, int *out);
+cudaError_t resident_blocks(const void *fn, int threads, int device, int *out,
+                            size_t dyn_smem = 0);
 
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bool vec,
                           int device, cudaStream_t s);
 cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec,
-                        int device, cudaStream_t s);
+                        const ErrorSink &sink, int device, cudaStream_t s);
 cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s);
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s);
 cudaError_t launch_ring(const RingParams &p, cudaStream_t s);

@@ -9,25 +9,30 @@
 // flight per thread), reduces in registers in ascending rank order, and
 // stores the result to every destination.  HBM traffic is the algorithmic
 // minimum: P reads and (number of outputs) writes per vector position.
+// Inputs are read once, so their loads carry the evict-first (streaming) cache
+// policy; results use the normal policy because the usual next consumer (the
+// AllGather after a ReduceScatter) reads them straight back.
 //
 // Grid: blockIdx.y is the job (1 for AllReduce, P for ReduceScatter), and
 // blockIdx.x strides over the job's vectors; the launcher caps the grid at
 // the number of blocks the SMs hold at once, so every block is resident.
 #include "dt_internal.h"
+#include "dt_device.cuh"
 #include "dt_math.cuh"
 
 namespace dt {
 namespace {
 
 template <int PMAX>
-struct Unroll {   // 16 loads of 16 bytes in flight per thread
-    static constexpr int U = PMAX >= 16 ? 1 : 16 / PMAX;
+struct Unroll {   // 8 loads of 16 bytes in flight per thread (16 at P > 8)
+    static constexpr int U = PMAX >= 8 ? 1 : 8 / PMAX;
 };
 
 template <int DT, int OP, int PMAX>
 __global__ void __launch_bounds__(kThreads)
 reduce_vec_kernel(const __grid_constant__ ReduceParams p)
 {
+    pdl_begin();
     constexpr int U = Unroll<PMAX>::U;
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     const int P = p.P;
@@ -47,7 +52,7 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
             if (v < nvec) {
 #pragma unroll
                 for (int r = 0; r < PMAX; ++r)
-                    if (r < P) x[u][r] = __ldcg(static_cast<const uint4 *>(p.in[r]) + in_off + v);
+                    if (r < P) x[u][r] = __ldcs(static_cast<const uint4 *>(p.in[r]) + in_off + v);
             }
         }
 #pragma unroll
@@ -73,6 +78,7 @@ template <int DT, int OP>
 __global__ void __launch_bounds__(kThreads)
 reduce_scalar_kernel(const __grid_constant__ ReduceParams p)
 {
+    pdl_begin();
     const int j = blockIdx.y;
     const uint64_t in_elem_off = (uint64_t)j * p.job_stride;
     void *const *dst = p.out + j * p.out_per_job;
@@ -140,9 +146,7 @@ cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bo
     if (cap < 1) cap = 1;
     const unsigned gx = (unsigned)(want < cap ? want : cap);
 
-    count_launch();
-    k.fn<<<dim3(gx, (unsigned)jobs), kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k.fn, dim3(gx, (unsigned)jobs), dim3(kThreads), 0, s, false, p);
 }
 
 }  // namespace dt
