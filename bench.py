@@ -252,14 +252,31 @@ def measure_rows(dt, dev, peak):
                       "frac_of_measured_hbm": round(gbs / peak, 4),
                       "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4), **extra}
 
-    # A1: AllReduce kSum, P=2, fp32 2^20 per rank (16 MiB moved: L2-resident, launch-bound)
+    # A1: AllReduce kSum, P=2, fp32 2^20 per rank (16 MiB moved: L2-resident,
+    # launch-bound): per-call device time from a replayed CUDA graph of 100
+    # calls, and per call when issued one by one from Python
     w = workloads.allreduce_small()
     xs = [x.to(dev) for x in w.inputs]
     outs = [torch.empty_like(x) for x in xs]
     g = dt.dt_group_create(2, dev.index)
     n = xs[0].numel()
-    ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 200)
-    rec("allreduce_sum_f32_P2_n2^20", 2 * 2 * n * 4, ms, l2_resident=True)
+    ms_stream = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 200)
+    ms_graph = None
+    try:
+        st = torch.cuda.Stream(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(graph, stream=st):
+                for _ in range(100):
+                    dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum", 0, st)
+        graph.replay()
+        torch.cuda.synchronize()
+        ms_graph = time_events(graph.replay, 20) / 100
+    except Exception:
+        ms_graph = None
+    rec("allreduce_sum_f32_P2_n2^20", 2 * 2 * n * 4, ms_graph if ms_graph else ms_stream,
+        l2_resident=True, timing="CUDA graph of 100 calls" if ms_graph else "per call",
+        us_per_call_issued_from_python=round(ms_stream * 1e3, 2))
     dt.dt_group_destroy(g)
     del xs, outs
 
@@ -321,9 +338,10 @@ def measure_rows(dt, dev, peak):
         dt.dt_barrier(g)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    raw = torch.cuda.current_stream(dev).cuda_stream
     s.record()
     for _ in range(calls):
-        dt.dt_barrier(g)
+        dt.dt_barrier(g, ALL, raw)
     e.record()
     torch.cuda.synchronize()
     us_direct = s.elapsed_time(e) * 1e3 / calls
@@ -356,6 +374,65 @@ def measure_rows(dt, dev, peak):
     return rows
 
 
+def run_e2e(dt, g, xs, P, rows_, cols, m, steps, world, dev):
+    """Pipelined end-to-end steps; returns (ms, GB/s, h2d bytes, d2h bytes)."""
+    import torch
+    ALL = dt.DT_ALL_RANKS
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h_in = [x.cpu().pin_memory() for x in xs]
+    sets = []
+    for _ in range(2):
+        sets.append({
+            "in": [torch.empty_like(x) for x in xs],
+            "rs": [torch.empty(rows_ // P, cols, dtype=torch.bfloat16, device=dev) for _ in range(P)],
+            "ag": [torch.empty(rows_, cols, dtype=torch.bfloat16, device=dev) for _ in range(P)],
+            "h_out": [torch.empty(rows_, cols, dtype=torch.bfloat16).pin_memory() for _ in range(P)],
+            "ev_in": torch.cuda.Event(), "ev_done": torch.cuda.Event(), "ev_out": torch.cuda.Event(),
+        })
+    raw = comp.cuda_stream
+
+    def one(i):
+        st = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(st["ev_done"])          # step i-2 is done reading this set
+            for d, h in zip(st["in"], h_in):
+                d.copy_(h, non_blocking=True)
+            st["ev_in"].record(s_in)
+        comp.wait_event(st["ev_in"])
+        if i >= 2:
+            comp.wait_event(st["ev_out"])               # step i-2's outputs have left
+        dt.dt_barrier(g, ALL, raw)
+        dt.dt_reduce_scatter(g, ALL, st["in"], st["rs"], m, "bf16", "avg", raw)
+        dt.dt_barrier(g, ALL, raw)
+        dt.dt_all_gather(g, ALL, st["rs"], st["ag"], None, rows_ // P, cols * 2, 0, raw)
+        st["ev_done"].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(st["ev_done"])
+            for h, d in zip(st["h_out"], st["ag"]):
+                h.copy_(d, non_blocking=True)
+            st["ev_out"].record(s_out)
+
+    for i in range(4):                                   # warm-up
+        one(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    s_in.wait_stream(comp)
+    s_out.wait_stream(comp)
+    for i in range(steps):
+        one(i)
+    comp.wait_stream(s_out)
+    t1.record(comp)
+    torch.cuda.synchronize()
+    rs_b, ag_b = step_bytes(P, rows_, cols)
+    ms, value = aggregate(t0.elapsed_time(t1), (rs_b + ag_b) * steps, world, dev)
+    h2d = sum(x.numel() * 2 for x in xs)
+    d2h = sum(x.numel() * 2 for x in sets[0]["ag"])
+    return ms, value, h2d, d2h
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -378,24 +455,25 @@ def run_ours(args):
     rs_b, ag_b = step_bytes()
     stream = torch.cuda.current_stream(dev)
 
+    raw = stream.cuda_stream
+
     def step(ev=None):
-        dt.dt_barrier(g)
+        dt.dt_barrier(g, ALL, raw)
         if ev is not None:
             ev[0].record()
-        dt.dt_reduce_scatter(g, ALL, xs, rs, m, "bf16", "avg")
+        dt.dt_reduce_scatter(g, ALL, xs, rs, m, "bf16", "avg", raw)
         if ev is not None:
             ev[1].record()
-        dt.dt_barrier(g)
+        dt.dt_barrier(g, ALL, raw)
         if ev is not None:
             ev[2].record()
-        dt.dt_all_gather(g, ALL, rs, ag, None, rows_ // P, cols * 2)
+        dt.dt_all_gather(g, ALL, rs, ag, None, rows_ // P, cols * 2, 0, raw)
         if ev is not None:
             ev[3].record()
 
     for _ in range(args.warmup):
         step()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -403,11 +481,14 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # timed region: K back-to-back steps, nothing between the launches, so the
+    # kernels' programmatic dependent launches overlap each launch with the
+    # previous kernel's tail
     launches0 = dt.dt_launch_count()
     wall0 = time.time()
     t_start.record()
-    for i in range(K):
-        step(evs[i])
+    for _ in range(K):
+        step()
     t_end.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -418,56 +499,49 @@ def run_ours(args):
     clocks.stop()
     local_ms = t_start.elapsed_time(t_end)
     ms, value = aggregate(local_ms, (rs_b + ag_b) * K, world, dev)
-    rs_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-    ag_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+
+    # per-kernel durations: a second pass with a CUDA event pair around each
+    # ReduceScatter and AllGather launch; the events serialise the launches
+    # (no overlap with the neighbouring kernels), so these are upper bounds
+    K2 = min(K, 2000)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K2)]
+    torch.cuda.synchronize()
+    for i in range(K2):
+        step(evs[i])
+    torch.cuda.synchronize()
+    rs_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K2
+    ag_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K2
     assert dt.dt_group_check(g) == dt.DT_OK
 
     if rs_ms >= ag_ms:
         dom, dom_bytes, dom_ms, key = "reduce_scatter (reduce_vec_kernel<bf16,avg,P<=4>)", rs_b, rs_ms, "reduce_scatter"
     else:
-        dom, dom_bytes, dom_ms, key = "all_gather (copy_vec_kernel)", ag_b, ag_ms, "all_gather"
+        dom, dom_bytes, dom_ms, key = "all_gather (copy_bulk_kernel, TMA)", ag_b, ag_ms, "all_gather"
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(key),
                 "kernel": dom, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": round(dom_ms * 1e3, 2),
+                "timing": f"CUDA events around each launch over {K2} steps (serialised launches)",
                 "per_kernel": {
                     "reduce_scatter": {"bytes": rs_b, "avg_us": round(rs_ms * 1e3, 2),
                                        "GB/s": round(rs_b / (rs_ms * 1e-3) / 1e9, 1)},
                     "all_gather": {"bytes": ag_b, "avg_us": round(ag_ms * 1e3, 2),
                                    "GB/s": round(ag_b / (ag_ms * 1e-3) / 1e9, 1)}}}
 
-    # e2e: same step through the public API, inputs from pinned host memory and
-    # the gathered result read back, copies inside the timed region
-    h_in = [x.cpu().pin_memory() for x in xs]
-    h_out = [torch.empty(rows_, cols, dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    # e2e: the same step through the public API with every step's four inputs
+    # copied in from pinned host memory and its four gathered outputs copied
+    # back, inside the timed region.  Steps are software-pipelined over two
+    # device buffer sets: the inputs of step i+1 travel host->device and the
+    # outputs of step i device->host (each on its own stream) while step i or
+    # i+1 computes.
     e2e_steps = max(3, min(K, 50))
-
-    def e2e_step():
-        for d, h in zip(xs, h_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(h_out, ag):
-            h.copy_(d, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
-    s1.record()
-    torch.cuda.synchronize()
-    e2e_ms, e2e_value = aggregate(s0.elapsed_time(s1), (rs_b + ag_b) * e2e_steps, world, dev)
-    h2d = sum(x.numel() * 2 for x in xs)
-    d2h = sum(x.numel() * 2 for x in ag)
+    e2e_ms, e2e_value, h2d, d2h = run_e2e(dt, g, xs, P, rows_, cols, m, e2e_steps, world, dev)
 
     rows_out = None
     if args.rows and world == 1:
         dt.dt_group_destroy(g)
         g = None
-        del h_in, h_out
         rows_out = measure_rows(dt, dev, peak)
 
     cpu = None
@@ -497,7 +571,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": round(e2e_ms / e2e_steps, 4)},
+                    "ms_per_step": round(e2e_ms / e2e_steps, 4),
+                    "pipeline": "two buffer sets; H2D, step and D2H on three streams"},
             "gpu_launches": launches,
             "clocks": clocks.summary(wall0, wall1),
         }
@@ -509,6 +584,107 @@ def run_ours(args):
     return 0
 
 
+def run_sweep(args):
+    """Every op at per-rank sizes 4 KiB .. 1 GiB (x4), P in {2, 4, 8, 16},
+    fp32/bf16/int32, kSum/kMax: one JSON line per point on stdout.  Each point
+    is a CUDA graph of back-to-back calls (no host gaps between launches),
+    replayed and timed with CUDA events; points whose working set (inputs plus
+    outputs) fits in L2 are marked "l2_resident"."""
+    import torch
+    from same_device_collective_gb300 import dt, workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = measured_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ALL = dt.DT_ALL_RANKS
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32}
+    ranks = [int(x) for x in args.sweep_ranks.split(",")]
+    sizes = [b for b in workloads.SWEEP_BYTES if b <= args.sweep_max_bytes]
+    cap_stream = torch.cuda.Stream(dev)
+    raw = cap_stream.cuda_stream
+
+    def timed(fn, ws):
+        calls = 100 if ws < (64 << 20) else (20 if ws < (4 << 30) else 5)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            fn()                                   # first call outside the capture
+            with torch.cuda.graph(graph, stream=cap_stream):
+                for _ in range(calls):
+                    fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            graph.replay()
+            s1.record()
+            s1.synchronize()
+            ts.append(s0.elapsed_time(s1) / calls)
+        del graph
+        ts.sort()
+        return ts[1]
+
+    def emit(op, P, dtype, redop, nbytes, outputs, ms, alg_bytes, ws):
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"sweep": op, "P": P, "dtype": dtype, "op": redop,
+                          "bytes_per_rank": nbytes, "outputs": outputs,
+                          "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                          "frac_of_measured": round(gbs / peak, 4),
+                          "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                          "l2_resident": ws <= l2}), flush=True)
+
+    for P in ranks:
+        g = dt.dt_group_create(P, 0)
+        for nbytes in sizes:
+            for dtype in ["f32", "bf16", "i32"]:
+                w = workloads.sweep_inputs(4, P, nbytes, dtype, device=str(dev))
+                xs = w.inputs
+                n = xs[0].numel()
+                es = 2 if dtype == "bf16" else 4
+                free = torch.cuda.mem_get_info(dev)[0]
+                per_rank = P * nbytes <= 0.6 * free
+                outs = [torch.empty_like(x) for x in xs] if per_rank else [torch.empty_like(xs[0])] * P
+                flags = 0 if per_rank else dt.DT_SHARED_OUTPUT
+                m = n // P
+                rs = [torch.empty(m, dtype=tdt[dtype], device=dev) for _ in range(P)]
+                for redop in ["sum", "max"]:
+                    ar_bytes = (2 * P if per_rank else P + 1) * n * es
+                    ms = timed(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, dtype, redop, flags, raw),
+                               ar_bytes)
+                    emit("allreduce", P, dtype, redop, nbytes, "per-rank" if per_rank else "shared",
+                         ms, ar_bytes, ar_bytes)
+                    rs_bytes = (P + 1) * n * es
+                    ms = timed(lambda: dt.dt_reduce_scatter(g, ALL, xs, rs, m, dtype, redop, raw),
+                               rs_bytes)
+                    emit("reduce_scatter", P, dtype, redop, nbytes, "per-rank", ms, rs_bytes, rs_bytes)
+                del outs, rs
+                if dtype == "i32":
+                    a2a = [torch.empty_like(x) for x in xs]
+                    ms = timed(lambda: dt.dt_all_to_all(g, ALL, xs, a2a, nbytes // P, raw), 2 * P * nbytes)
+                    emit("all_to_all", P, "bytes", None, nbytes, "per-rank", ms, 2 * P * nbytes,
+                         2 * P * nbytes)
+                    del a2a
+                    free = torch.cuda.mem_get_info(dev)[0]
+                    per_rank = P * P * nbytes <= 0.6 * free
+                    if per_rank:
+                        ag = [torch.empty(P * n, dtype=torch.int32, device=dev) for _ in range(P)]
+                    else:
+                        ag = [torch.empty(P * n, dtype=torch.int32, device=dev)] * P
+                    ag_bytes = (P + P * P if per_rank else 2 * P) * nbytes
+                    ms = timed(lambda: dt.dt_all_gather(g, ALL, xs, ag, None, 1, nbytes,
+                                                        0 if per_rank else dt.DT_SHARED_OUTPUT, raw),
+                               ag_bytes)
+                    emit("all_gather", P, "bytes", None, nbytes, "per-rank" if per_rank else "shared",
+                         ms, ag_bytes, ag_bytes)
+                    del ag
+                del w, xs
+                torch.cuda.empty_cache()
+        assert dt.dt_group_check(g) == dt.DT_OK
+        dt.dt_group_destroy(g)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -517,11 +693,17 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", dest="rows", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-op size sweep (one JSON line per point) instead of the step")
+    ap.add_argument("--sweep-ranks", default="2,4,8,16")
+    ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

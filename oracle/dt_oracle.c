@@ -267,6 +267,24 @@ int orc_all_gather(int P, const void *const *in, void *const *out, const size_t 
     return ORC_OK;
 }
 
+/* The one concatenation of the AllGather above, written to a single buffer
+ * (every rank's output holds exactly this). */
+int orc_all_gather_one(int P, const void *const *in, void *out, const size_t *rows,
+                       size_t row_bytes)
+{
+    if (P < 1 || P > ORC_MAX_RANKS || !rows)
+        return ORC_INVALID;
+    size_t offset_rows = 0;
+    for (int r = 0; r < P; r++) {
+        const unsigned char *src = in[r];
+        unsigned char *dst = (unsigned char *)out + offset_rows * row_bytes;
+        for (size_t b = 0; b < rows[r] * row_bytes; b++)
+            dst[b] = src[b];
+        offset_rows += rows[r];
+    }
+    return ORC_OK;
+}
+
 /* S -> S ([DT] §2.1 AllToAll, split and concatenated along dim 0): rank i's
  * input is P chunks of chunk_bytes; chunk j goes to rank j, which stacks the
  * chunks it receives in ascending source rank:

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.orc_reduce_scatter.argtypes = [i, i, i, vpp, vpp, sz]
         L.orc_all_gather.argtypes = [i, vpp, vpp, szp, sz]
         L.orc_all_to_all.argtypes = [i, vpp, vpp, sz]
+        L.orc_all_gather_one.argtypes = [i, vpp, vp, szp, sz]
         L.orc_bucket_plan.argtypes = [szp, sz, sz, sz, szp, szp]
         L.orc_bucket_allreduce.argtypes = [i, i, i, vpp, szp, sz]
         L.orc_barrier_sim.argtypes = [i, i, ctypes.POINTER(ctypes.c_int32),
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.orc_bf16_to_f32.restype = ctypes.c_float
         L.orc_f32_to_bf16_array.argtypes = [vp, vp, sz]
         for name in ("orc_reduce", "orc_allreduce", "orc_reduce_scatter", "orc_all_gather",
+                     "orc_all_gather_one",
                      "orc_all_to_all", "orc_bucket_plan", "orc_bucket_allreduce",
                      "orc_barrier_sim"):
             getattr(L, name).restype = ctypes.c_int
@@ -161,6 +163,17 @@ def all_gather(inputs: Sequence[np.ndarray], rows: Sequence[int] | None = None,
     outs = [np.empty(total, dtype=np.uint8) for _ in range(P)]
     _check(lib().orc_all_gather(P, _ptrs(ins), _ptrs(outs), rows_c, row_bytes), "all_gather")
     return outs
+
+
+def all_gather_one(inputs: Sequence[np.ndarray], rows: Sequence[int], row_bytes: int) -> np.ndarray:
+    """The single concatenation that every rank receives (uint8)."""
+    ins = [np.ascontiguousarray(a).reshape(-1).view(np.uint8) for a in inputs]
+    P = len(ins)
+    rows_c = (ctypes.c_size_t * P)(*rows)
+    out = np.empty(sum(rows) * row_bytes, dtype=np.uint8)
+    _check(lib().orc_all_gather_one(P, _ptrs(ins), out.ctypes.data, rows_c, row_bytes),
+           "all_gather_one")
+    return out
 
 
 def all_to_all(inputs: Sequence[np.ndarray]) -> list:

@@ -349,6 +349,17 @@ def test_uneven_all_gather_row_offsets_closed_form():
     assert outs[0][4 * row_bytes] == 3
 
 
+def test_all_gather_one_equals_every_rank_output():
+    rows = [3, 0, 5, 2]
+    xs = [rng.integers(0, 255, c * 8, dtype=np.uint8) for c in rows]
+    full = oracle.all_gather(xs, rows, 8)
+    one = oracle.all_gather_one(xs, rows, 8)
+    ref = torch.cat([torch.from_numpy(x) for x in xs]).numpy()
+    assert np.array_equal(one, ref)
+    for o in full:
+        assert np.array_equal(o, one)
+
+
 def test_uneven_with_equal_rows_equals_equal_gather():
     P, rows, rb = 4, 3, 20
     xs = [rng.integers(0, 255, rows * rb, dtype=np.uint8) for _ in range(P)]
