@@ -222,8 +222,11 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-def time_events(fn, iters, warmup=3):
-    """Median ms of fn over iters, CUDA events on the current stream."""
+def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
+    """Median ms of fn over iters, CUDA events on the current stream.  Before
+    each timed call the GPU is kept busy (a ~2 ms sleep kernel) so that the
+    host has enqueued all of fn's work before the start event fires: the
+    interval then measures device time, not host marshalling."""
     import torch
     for _ in range(warmup):
         fn()
@@ -231,6 +234,7 @@ def time_events(fn, iters, warmup=3):
     en = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
     torch.cuda.synchronize()
     for i in range(iters):
+        torch.cuda._sleep(lead_cycles)
         st[i].record()
         fn()
         en[i].record()
@@ -239,8 +243,13 @@ def time_events(fn, iters, warmup=3):
     return ts[len(ts) // 2]
 
 
-def measure_rows(dt, dev, peak):
-    """One measurement per collective at its own workload (device-resident)."""
+ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "uneven_all_gather",
+             "barrier"]
+
+
+def measure_rows(dt, dev, peak, only=None):
+    """One measurement per collective at its own workload (device-resident).
+    `only` restricts it to one of ROW_NAMES."""
     import torch
     from same_device_collective_gb300 import workloads
     rows = {}
@@ -252,124 +261,134 @@ def measure_rows(dt, dev, peak):
                       "frac_of_measured_hbm": round(gbs / peak, 4),
                       "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4), **extra}
 
+    def want(name):
+        return only is None or only == name
+
     # A1: AllReduce kSum, P=2, fp32 2^20 per rank (16 MiB moved: L2-resident,
     # launch-bound): per-call device time from a replayed CUDA graph of 100
     # calls, and per call when issued one by one from Python
-    w = workloads.allreduce_small()
-    xs = [x.to(dev) for x in w.inputs]
-    outs = [torch.empty_like(x) for x in xs]
-    g = dt.dt_group_create(2, dev.index)
-    n = xs[0].numel()
-    ms_stream = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 200)
-    ms_graph = None
-    try:
-        st = torch.cuda.Stream(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(st):
-            with torch.cuda.graph(graph, stream=st):
-                for _ in range(100):
-                    dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum", 0, st)
-        graph.replay()
-        torch.cuda.synchronize()
-        ms_graph = time_events(graph.replay, 20) / 100
-    except Exception:
+    if want("allreduce_small"):
+        w = workloads.allreduce_small()
+        xs = [x.to(dev) for x in w.inputs]
+        outs = [torch.empty_like(x) for x in xs]
+        g = dt.dt_group_create(2, dev.index)
+        n = xs[0].numel()
+        ms_stream = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 200)
         ms_graph = None
-    rec("allreduce_sum_f32_P2_n2^20", 2 * 2 * n * 4, ms_graph if ms_graph else ms_stream,
-        l2_resident=True, timing="CUDA graph of 100 calls" if ms_graph else "per call",
-        us_per_call_issued_from_python=round(ms_stream * 1e3, 2))
-    dt.dt_group_destroy(g)
-    del xs, outs
+        try:
+            st = torch.cuda.Stream(dev)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(graph, stream=st):
+                    for _ in range(100):
+                        dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum", 0, st)
+            graph.replay()
+            torch.cuda.synchronize()
+            ms_graph = time_events(graph.replay, 20) / 100
+        except Exception:
+            ms_graph = None
+        rec("allreduce_sum_f32_P2_n2^20", 2 * 2 * n * 4, ms_graph if ms_graph else ms_stream,
+            l2_resident=True, timing="CUDA graph of 100 calls" if ms_graph else "per call",
+            us_per_call_issued_from_python=round(ms_stream * 1e3, 2))
+        dt.dt_group_destroy(g)
+        del xs, outs
 
     # A1 at bandwidth scale: AllReduce kSum P=8 fp32, 64 MiB per rank
-    n = 16 << 20
-    gen = torch.Generator(device=dev).manual_seed(4)
-    xs = [torch.rand(n, generator=gen, device=dev) for _ in range(8)]
-    outs = [torch.empty_like(x) for x in xs]
-    g = dt.dt_group_create(8, dev.index)
-    ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 20)
-    rec("allreduce_sum_f32_P8_64MiB", 2 * 8 * n * 4, ms)
-    dt.dt_group_destroy(g)
-    del xs, outs
+    if want("allreduce_large"):
+        n = 16 << 20
+        gen = torch.Generator(device=dev).manual_seed(4)
+        xs = [torch.rand(n, generator=gen, device=dev) for _ in range(8)]
+        outs = [torch.empty_like(x) for x in xs]
+        g = dt.dt_group_create(8, dev.index)
+        ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 20)
+        rec("allreduce_sum_f32_P8_64MiB", 2 * 8 * n * 4, ms)
+        dt.dt_group_destroy(g)
+        del xs, outs
 
     # A5: fused bucket all-reduce kAvg, P=8, 200 bf16 gradients, 25 MiB buckets
-    w = workloads.bucket_grads(device=str(dev))
-    counts = w.meta["counts"]
-    g = dt.dt_group_create(8, dev.index)
-    _, nb = dt.dt_bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
-    ms = time_events(lambda: dt.dt_bucket_allreduce(g, w.inputs, counts, "bf16", "avg",
-                                                    workloads.BUCKET_CAP_BYTES), 20)
-    rec("bucket_allreduce_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
-        barriers=nb - 1)
-    dt.dt_group_destroy(g)
-    del w
+    if want("bucket"):
+        w = workloads.bucket_grads(device=str(dev))
+        counts = w.meta["counts"]
+        g = dt.dt_group_create(8, dev.index)
+        _, nb = dt.dt_bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
+        ms = time_events(lambda: dt.dt_bucket_allreduce(g, w.inputs, counts, "bf16", "avg",
+                                                        workloads.BUCKET_CAP_BYTES), 20)
+        rec("bucket_allreduce_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
+            barriers=nb - 1)
+        dt.dt_group_destroy(g)
+        del w
 
     # A4: AllToAll P=8, bf16 [65536, 4096] per rank
-    w = workloads.all_to_all_tokens(device=str(dev))
-    outs = [torch.empty_like(x) for x in w.inputs]
-    g = dt.dt_group_create(8, dev.index)
-    nbytes_rank = w.inputs[0].numel() * 2
-    ms = time_events(lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes_rank // 8), 10)
-    rec("all_to_all_bf16_P8_65536x4096", 2 * 8 * nbytes_rank, ms)
-    dt.dt_group_destroy(g)
-    del w, outs
+    if want("all_to_all"):
+        w = workloads.all_to_all_tokens(device=str(dev))
+        outs = [torch.empty_like(x) for x in w.inputs]
+        g = dt.dt_group_create(8, dev.index)
+        nbytes_rank = w.inputs[0].numel() * 2
+        ms = time_events(lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes_rank // 8), 10)
+        rec("all_to_all_bf16_P8_65536x4096", 2 * 8 * nbytes_rank, ms)
+        dt.dt_group_destroy(g)
+        del w, outs
 
     # A3b: uneven AllGather P=8, int32 rows U[1,16384] x 4096 (per-rank outputs)
-    w = workloads.uneven_gather(device=str(dev))
-    rws = w.meta["rows"]
-    total = sum(rws)
-    outs = [torch.empty(total, 4096, dtype=torch.int32, device=dev) for _ in range(8)]
-    g = dt.dt_group_create(8, dev.index)
-    ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4), 10)
-    rec("uneven_all_gather_i32_P8", total * 16384 * (1 + 8), ms, rows=rws)
-    dt.dt_group_destroy(g)
-    del outs
-    shared = torch.empty(total, 4096, dtype=torch.int32, device=dev)
-    g = dt.dt_group_create(8, dev.index)
-    ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, [shared] * 8, rws, 0, 4096 * 4,
-                                              flags=dt.DT_SHARED_OUTPUT), 10)
-    rec("uneven_all_gather_i32_P8_shared_output", total * 16384 * 2, ms)
-    dt.dt_group_destroy(g)
-    del w, shared
+    if want("uneven_all_gather"):
+        w = workloads.uneven_gather(device=str(dev))
+        rws = w.meta["rows"]
+        total = sum(rws)
+        outs = [torch.empty(total, 4096, dtype=torch.int32, device=dev) for _ in range(8)]
+        g = dt.dt_group_create(8, dev.index)
+        ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4), 10)
+        rec("uneven_all_gather_i32_P8", total * 16384 * (1 + 8), ms, rows=rws)
+        dt.dt_group_destroy(g)
+        del outs
+        shared = torch.empty(total, 4096, dtype=torch.int32, device=dev)
+        g = dt.dt_group_create(8, dev.index)
+        ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, [shared] * 8, rws, 0, 4096 * 4,
+                                                  flags=dt.DT_SHARED_OUTPUT), 10)
+        rec("uneven_all_gather_i32_P8_shared_output", total * 16384 * 2, ms)
+        dt.dt_group_destroy(g)
+        del w, shared
 
     # A6: barrier latency, P=16, 10^5 back-to-back calls (and as a replayed CUDA graph)
-    g = dt.dt_group_create(16, dev.index)
-    calls = 100_000
-    for _ in range(100):
-        dt.dt_barrier(g)
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    raw = torch.cuda.current_stream(dev).cuda_stream
-    s.record()
-    for _ in range(calls):
-        dt.dt_barrier(g, ALL, raw)
-    e.record()
-    torch.cuda.synchronize()
-    us_direct = s.elapsed_time(e) * 1e3 / calls
-    us_graph = None
-    try:
-        stream = torch.cuda.Stream(dev)
-        per_graph = 1000
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
-                for _ in range(per_graph):
-                    dt.dt_barrier(g, stream=stream)
+    if want("barrier"):
+        g = dt.dt_group_create(16, dev.index)
+        calls = 100_000
+        for _ in range(100):
+            dt.dt_barrier(g)
         torch.cuda.synchronize()
-        graph.replay()
-        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        raw = torch.cuda.current_stream(dev).cuda_stream
         s.record()
-        for _ in range(calls // per_graph):
-            graph.replay()
+        for _ in range(calls):
+            dt.dt_barrier(g, ALL, raw)
         e.record()
         torch.cuda.synchronize()
-        us_graph = s.elapsed_time(e) * 1e3 / calls
-    except Exception as ex:   # capture support is reported, not required
-        us_graph = f"capture failed: {type(ex).__name__}"
-    win_ok = dt.dt_group_check(g) == dt.DT_OK
-    dt.dt_group_destroy(g)
-    rows["barrier_P16"] = {"us_per_call_stream": round(us_direct, 3),
-                           "us_per_call_graph": us_graph if isinstance(us_graph, str)
-                           else round(us_graph, 3), "calls": calls, "status_ok": win_ok}
+        us_direct = s.elapsed_time(e) * 1e3 / calls
+        us_graph = None
+        try:
+            stream = torch.cuda.Stream(dev)
+            per_graph = 1000
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    for _ in range(per_graph):
+                        dt.dt_barrier(g, stream=stream)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            s.record()
+            for _ in range(calls // per_graph):
+                graph.replay()
+            e.record()
+            torch.cuda.synchronize()
+            us_graph = s.elapsed_time(e) * 1e3 / calls
+        except Exception as ex:   # capture support is reported, not required
+            us_graph = f"capture failed: {type(ex).__name__}"
+        win_ok = dt.dt_group_check(g) == dt.DT_OK
+        dt.dt_group_destroy(g)
+        rows["barrier_P16"] = {"us_per_call_stream": round(us_direct, 3),
+                               "us_per_call_graph": us_graph if isinstance(us_graph, str)
+                               else round(us_graph, 3), "calls": calls, "status_ok": win_ok}
+
     torch.cuda.empty_cache()
     return rows
 
@@ -697,6 +716,8 @@ def main(argv=None):
                     help="per-op size sweep (one JSON line per point) instead of the step")
     ap.add_argument("--sweep-ranks", default="2,4,8,16")
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
+    ap.add_argument("--row", choices=ROW_NAMES,
+                    help="measure one collective at its own workload and print it")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -704,6 +725,13 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.row:
+        import torch
+        from same_device_collective_gb300 import dt
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"rows": measure_rows(dt, dev, measured_peak()[0], only=args.row)}))
+        return 0
     return run_ours(args)
 
 

@@ -199,11 +199,12 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
  *   world_size        P (1..DT_MAX_RANKS); no group is needed
  *   grads, counts, n_tensors, dtype, op, bucket_cap_bytes, stream
  *                     as dt_bucket_allreduce; the results are identical
- * The chunk and pointer tables live in one fixed 1 MiB device array inside
+ * The tensor and pointer tables live in one fixed 1 MiB device array inside
  * this library (every GPU that loads the library holds it until the process
  * exits) and are staged from a fixed host array: the call allocates nothing.
- * Tables that do not fit (n_tensors * P * 8 bytes of pointers plus 16 bytes
- * per 32768-element chunk) return DT_ERR_TOO_LARGE before anything is
+ * Tables that do not fit (n_tensors * (P * 8 + 24) bytes plus 4 bytes per
+ * thread block of every bucket, at most a few hundred blocks per bucket) or
+ * more than 4096 buckets return DT_ERR_TOO_LARGE before anything is
  * enqueued.  Every call shares the array and leaves its contents behind;
  * calls that overlap on the GPU (unordered streams) race on it, calls on one
  * stream do not.  No signal barrier runs between buckets (there is no group

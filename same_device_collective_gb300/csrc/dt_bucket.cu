@@ -5,10 +5,12 @@
 // group and then divides each gradient view by the replicate world size; DDP
 // (PyTorch communication page §六.5) gathers gradients into 25 MB buckets so
 // that one bandwidth-bound call replaces many latency-bound ones.  Here the
-// bucket is never flattened: the host hands the kernel a chunk table (tensor
-// slot, element range) and a table of the P rank pointers of every tensor, and
-// each block reduces its chunks in place in every rank's gradient, reading
-// each element once per rank and writing it once per rank.
+// bucket is never flattened into a copy: the host hands the kernel a table of
+// the bucket's tensors (their place in the bucket's flattened element space)
+// and the P rank pointers of each, and every block reduces an equal,
+// contiguous slice of that space in place in every rank's gradient, reading
+// each element once per rank and writing it once per rank.  Equal slices keep
+// the blocks balanced however uneven the tensor sizes are.
 #include "dt_internal.h"
 #include "dt_device.cuh"
 #include "dt_math.cuh"
@@ -26,53 +28,56 @@ __global__ void __launch_bounds__(kThreads)
 bucket_kernel(const __grid_constant__ BucketParams p)
 {
     constexpr int U = BucketUnroll<PMAX>::U;
-    constexpr int EPV = DT == DT_BF16 ? 8 : 4;
+    constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     __shared__ void *sp[DT_MAX_RANKS];
     const int P = p.P;
     pdl_begin();
 
-    for (uint32_t c = blockIdx.x; c < p.nchunks; c += gridDim.x) {
-        const BucketChunk ch = p.chunks[c];
-        const uint32_t slot = ch.slot & 0x7FFFFFFFu;
-        __syncthreads();   // the previous chunk is done with sp
+    const uint64_t lo = (uint64_t)blockIdx.x * p.per_block;
+    if (lo >= p.total) return;
+    const uint64_t hi = lo + p.per_block < p.total ? lo + p.per_block : p.total;
+
+    for (uint32_t t = p.block_start[blockIdx.x]; t < p.ntensors; ++t) {
+        const BucketTensor bt = p.tensors[t];
+        if (bt.first >= hi) break;
+        const uint64_t s = (lo > bt.first ? lo : bt.first) - bt.first;   // local range [s, e)
+        uint64_t e = hi - bt.first;
+        if (e > bt.count) e = bt.count;
+        if (s >= e) continue;                                              // only padding here
+        const uint32_t slot = bt.slot & 0x7FFFFFFFu;
+        __syncthreads();   // the previous tensor is done with sp
         if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)slot * P + threadIdx.x];
         __syncthreads();
 
-        if (ch.slot >> 31) {
-            const uint64_t nvec = ch.nelem / EPV;
-            const uint64_t v0 = ch.begin / EPV;   // chunk starts are multiples of EPV
-            const uint4 *in[PMAX];
-#pragma unroll
-            for (int r = 0; r < PMAX; ++r)
-                in[r] = r < P ? static_cast<const uint4 *>(sp[r]) + v0 : nullptr;
-            for (uint64_t base = threadIdx.x; base < nvec; base += (uint64_t)kThreads * U) {
+        uint64_t scalar_from = s;
+        if (bt.slot >> 31) {
+            const uint64_t vs = s / EPV, ve = e / EPV;   // s is a multiple of EPV
+            for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kThreads * U) {
                 uint4 x[U][PMAX];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const uint64_t v = base + (uint64_t)u * kThreads;
-                    if (v < nvec) {
+                    if (v < ve) {
 #pragma unroll
                         for (int r = 0; r < PMAX; ++r)
-                            if (r < P) x[u][r] = __ldcs(in[r] + v);
+                            if (r < P) x[u][r] = __ldcs(static_cast<const uint4 *>(sp[r]) + v);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const uint64_t v = base + (uint64_t)u * kThreads;
-                    if (v < nvec) {
+                    if (v < ve) {
                         const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
 #pragma unroll
                         for (int r = 0; r < PMAX; ++r)
-                            if (r < P) __stcs(static_cast<uint4 *>(sp[r]) + v0 + v, y);
+                            if (r < P) __stcs(static_cast<uint4 *>(sp[r]) + v, y);
                     }
                 }
             }
-            for (uint64_t i = nvec * EPV + threadIdx.x; i < ch.nelem; i += kThreads)
-                reduce_elem<DT, OP>(sp, 0, ch.begin + i, P, sp, P, p.avg_scale, p.avg_pow2);
-        } else {
-            for (uint64_t i = threadIdx.x; i < ch.nelem; i += kThreads)
-                reduce_elem<DT, OP>(sp, 0, ch.begin + i, P, sp, P, p.avg_scale, p.avg_pow2);
+            scalar_from = ve * EPV;   // ragged end of the tensor, if it is in this slice
         }
+        for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kThreads)
+            reduce_elem<DT, OP>(sp, 0, i, P, sp, P, p.avg_scale, p.avg_pow2);
     }
 }
 
@@ -87,19 +92,52 @@ BucketFn pick(int P)
     return bucket_kernel<DT, OP, 16>;
 }
 
+BucketFn pick_fn(int dtype, int op, int P)
+{
+    if (op != DT_AVG && op != DT_SUM) return nullptr;
+    if (dtype == DT_BF16) return op == DT_AVG ? pick<DT_BF16, DT_AVG>(P) : pick<DT_BF16, DT_SUM>(P);
+    if (dtype == DT_F32) return op == DT_AVG ? pick<DT_F32, DT_AVG>(P) : pick<DT_F32, DT_SUM>(P);
+    return nullptr;
+}
+
 }  // namespace
 
-cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s)
+uint64_t bucket_padded(uint64_t count, int dtype)
 {
-    BucketFn fn = nullptr;
-    if (dtype == DT_BF16) fn = op == DT_AVG ? pick<DT_BF16, DT_AVG>(p.P) : pick<DT_BF16, DT_SUM>(p.P);
-    else if (dtype == DT_F32) fn = op == DT_AVG ? pick<DT_F32, DT_AVG>(p.P) : pick<DT_F32, DT_SUM>(p.P);
-    if (!fn || (op != DT_AVG && op != DT_SUM)) return cudaErrorInvalidValue;
-    if (p.nchunks == 0) return cudaSuccess;
+    const uint64_t epv = dtype == DT_BF16 ? 8 : 4;
+    return (count + epv - 1) / epv * epv;
+}
+
+cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, uint32_t *blocks,
+                        uint64_t *per_block)
+{
+    BucketFn fn = pick_fn(dtype, op, P);
+    if (!fn) return cudaErrorInvalidValue;
     int resident = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
     if (e != cudaSuccess) return e;
-    const unsigned gx = p.nchunks < (uint32_t)resident ? p.nchunks : (unsigned)resident;
+    const uint64_t epv = dtype == DT_BF16 ? 8 : 4;
+    // at least one full pass of the block's threads per slice
+    const uint64_t min_slice = (uint64_t)kThreads * epv;
+    uint64_t g = (total + min_slice - 1) / min_slice;
+    if (g > (uint64_t)resident) g = resident;
+    if (g < 1) g = 1;
+    uint64_t per = (total + g - 1) / g;
+    per = (per + epv - 1) / epv * epv;
+    if (per == 0) per = epv;
+    *per_block = per;
+    *blocks = (uint32_t)((total + per - 1) / per);
+    if (*blocks == 0) *blocks = 1;
+    return cudaSuccess;
+}
+
+cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s)
+{
+    BucketFn fn = pick_fn(dtype, op, p.P);
+    if (!fn) return cudaErrorInvalidValue;
+    if (p.total == 0 || p.ntensors == 0) return cudaSuccess;
+    (void)device;
+    const unsigned gx = (unsigned)((p.total + p.per_block - 1) / p.per_block);
     return launch_kernel(fn, dim3(gx), dim3(kThreads), 0, s, false, p);
 }
 

@@ -590,7 +590,6 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     // validate and find overlapping gradient buffers (sorted sweep)
     std::vector<Range> ranges;
     ranges.reserve(n_tensors * P);
-    size_t nchunks = 0;
     for (size_t t = 0; t < n_tensors; ++t) {
         if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
         if (counts[t] == 0) continue;
@@ -599,13 +598,11 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
             if (!ptr) return DT_ERR_INVALID;
             ranges.push_back({(uintptr_t)ptr, (uintptr_t)ptr + counts[t] * es, p, 1});
         }
-        nchunks += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
     }
+    if (ranges.empty()) return DT_OK;
     std::sort(ranges.begin(), ranges.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
     for (size_t i = 1; i < ranges.size(); ++i)
         if (ranges[i].lo < ranges[i - 1].hi) return DT_ERR_INVALID;
-    if (nchunks == 0) return DT_OK;
-    if (nchunks > 0x7FFFFFFFu) return DT_ERR_INVALID;
 
     std::vector<size_t> bucket_of(n_tensors);
     const size_t nb = plan_buckets(counts, n_tensors, es, cap, bucket_of.data());
@@ -614,9 +611,35 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     if (!scope.ok) return DT_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // plan layout: [T * P pointers][chunks]; buckets own consecutive chunk runs
+    // per bucket: its tensors [tb, te), padded size, grid and slice length
+    struct BucketLaunch {
+        size_t tb, te;
+        uint64_t total, per_block;
+        uint32_t blocks;
+        size_t start_off;   // index of its first block_start entry
+    };
+    std::vector<BucketLaunch> bl(nb);
+    size_t n_starts = 0;
+    for (size_t b = 0, t = 0; b < nb; ++b) {
+        BucketLaunch &L = bl[b];
+        L.tb = t;
+        L.total = 0;
+        while (t < n_tensors && bucket_of[t] == b) L.total += dt::bucket_padded(counts[t++], dtype);
+        L.te = t;
+        L.blocks = 0;
+        L.per_block = 1;
+        if (L.total) {
+            cudaError_t e = dt::bucket_grid(dtype, op, P, L.total, g->device, &L.blocks, &L.per_block);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        L.start_off = n_starts;
+        n_starts += L.blocks;
+    }
+
+    // plan layout: [T * P pointers][T tensor entries][block starts]
     const size_t ptr_bytes = n_tensors * P * sizeof(void *);
-    const size_t plan_bytes = ptr_bytes + nchunks * sizeof(dt::BucketChunk);
+    const size_t tab_bytes = n_tensors * sizeof(dt::BucketTensor);
+    const size_t plan_bytes = ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t);
     const int k = g->next_plan;
     g->next_plan = (k + 1) % dt_group::kPlanSlots;
     cudaError_t e = cudaSuccess;
@@ -626,24 +649,25 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
 
     unsigned char *h = static_cast<unsigned char *>(g->h_plan[k]);
     memcpy(h, grads, ptr_bytes);
-    dt::BucketChunk *chunks = reinterpret_cast<dt::BucketChunk *>(h + ptr_bytes);
-    // buckets hold consecutive tensors, so chunks in tensor order are grouped
-    // by bucket; bucket_begin[b] is the first chunk of bucket b
-    std::vector<uint32_t> bucket_begin(nb + 1, 0);
-    for (size_t t = 0; t < n_tensors; ++t)
-        bucket_begin[bucket_of[t] + 1] +=
-            (uint32_t)((counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems);
-    for (size_t b = 0; b < nb; ++b) bucket_begin[b + 1] += bucket_begin[b];
-    size_t c = 0;
-    for (size_t t = 0; t < n_tensors; ++t) {
-        bool al = true;
-        for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
-        for (size_t beg = 0; beg < counts[t]; beg += dt::kBucketChunkElems) {
-            const size_t n = std::min<size_t>(dt::kBucketChunkElems, counts[t] - beg);
-            chunks[c].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
-            chunks[c].nelem = (uint32_t)n;
-            chunks[c].begin = beg;
-            ++c;
+    dt::BucketTensor *tab = reinterpret_cast<dt::BucketTensor *>(h + ptr_bytes);
+    uint32_t *starts = reinterpret_cast<uint32_t *>(h + ptr_bytes + tab_bytes);
+    for (const BucketLaunch &L : bl) {
+        uint64_t first = 0;
+        for (size_t t = L.tb; t < L.te; ++t) {
+            bool al = true;
+            for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
+            tab[t].first = first;
+            tab[t].count = counts[t];
+            tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
+            tab[t].pad = 0;
+            first += dt::bucket_padded(counts[t], dtype);
+        }
+        // block j starts at the last tensor (bucket-relative) with first <= j * per_block
+        size_t t = L.tb;
+        for (uint32_t j = 0; j < L.blocks; ++j) {
+            const uint64_t lo = (uint64_t)j * L.per_block;
+            while (t + 1 < L.te && tab[t + 1].first <= lo) ++t;
+            starts[L.start_off + j] = (uint32_t)(t - L.tb);
         }
     }
 
@@ -656,8 +680,12 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     bp.P = P;
     set_avg(P, &bp.avg_scale, &bp.avg_pow2);
     for (size_t b = 0; b < nb; ++b) {
-        bp.chunks = reinterpret_cast<const dt::BucketChunk *>(d + ptr_bytes) + bucket_begin[b];
-        bp.nchunks = bucket_begin[b + 1] - bucket_begin[b];
+        const BucketLaunch &L = bl[b];
+        bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
+        bp.block_start = reinterpret_cast<const uint32_t *>(d + ptr_bytes + tab_bytes) + L.start_off;
+        bp.ntensors = (uint32_t)(L.te - L.tb);
+        bp.total = L.total;
+        bp.per_block = L.per_block;
         e = dt::launch_bucket(bp, dtype, op, g->device, s);
         if (e != cudaSuccess) break;
         if (b + 1 < nb) {

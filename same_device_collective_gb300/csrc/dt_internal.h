@@ -16,7 +16,6 @@ namespace dt {
 
 constexpr int kThreads = 256;                          // threads per block, all data kernels
 constexpr int kMaxSeg = DT_MAX_RANKS * DT_MAX_RANKS;   // all-to-all: P^2 chunk copies
-constexpr uint32_t kBucketChunkElems = 32768;          // bucket work unit, elements
 
 // First device-side failure, written once (atomicCAS on code) by the kernel
 // that hit it, mirrored into host-mapped memory so the host can read it
@@ -76,23 +75,35 @@ struct CopyParams {
 };
 
 // ---- fused bucket all-reduce ----------------------------------------------
-// One chunk = up to kBucketChunkElems elements of one tensor.  slot indexes
-// the tensor's row of P pointers in `ptrs`; bit 31 of slot marks a tensor
-// whose P pointers are all 16-byte aligned (vector path).
-struct BucketChunk {
-    uint32_t slot;
-    uint32_t nelem;
-    uint64_t begin;
+// A bucket's tensors laid end to end form its flattened element space, in
+// which every tensor occupies its count rounded up to a whole 16-byte vector,
+// so that any boundary that is a multiple of the vector width is one inside
+// every tensor too.  Block b reduces the slice [b * per_block, (b + 1) *
+// per_block) of that space, starting at tensor block_start[b].
+struct BucketTensor {
+    uint64_t first;   // first element in the bucket's flattened space
+    uint64_t count;   // elements of the tensor
+    uint32_t slot;    // row of P pointers in `ptrs`; bit 31: all 16-byte aligned
+    uint32_t pad;
 };
 
 struct BucketParams {
-    const BucketChunk *chunks;
-    void *const *ptrs;   // [n_slots][P]
-    uint32_t nchunks;
+    const BucketTensor *tensors;     // this bucket's tensors, in order
+    const uint32_t *block_start;     // per block: index of its first tensor
+    void *const *ptrs;               // [n_slots][P]
+    uint64_t total;                  // padded elements in the bucket
+    uint64_t per_block;              // slice length, a multiple of the vector width
+    uint32_t ntensors;
     int32_t P;
     float avg_scale;
     int32_t avg_pow2;
 };
+
+// Elements a tensor occupies in the flattened space, and the grid the bucket
+// kernel uses for `total` such elements (blocks the SMs hold at once).
+uint64_t bucket_padded(uint64_t count, int dtype);
+cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, uint32_t *blocks,
+                        uint64_t *per_block);
 
 // ---- barrier ----------------------------------------------------------------
 struct BarrierParams {

@@ -5,7 +5,7 @@
 // device and bypasses their accounting), and code that runs while a stream
 // capture in global mode is active, where cudaMalloc is not permitted.  They
 // cannot create a dt_group, which allocates its window and plan scratch.
-// dt_bucket_allreduce_static serves them: the chunk and pointer tables that
+// dt_bucket_allreduce_static serves them: the tensor and pointer tables that
 // the bucket kernel reads live in a fixed file-scope device array of
 // kStaticScratchBytes, staged from a fixed host array, so a call allocates
 // nothing on the device or the host.
@@ -71,18 +71,15 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     const size_t es = dtype == DT_BF16 ? 2 : 4;
     const size_t cap = bucket_cap_bytes ? bucket_cap_bytes : DT_DEFAULT_BUCKET_CAP_BYTES;
 
-    // size check first: the tables must fit the fixed array
-    if (n_tensors > kStaticScratchBytes / (sizeof(void *) * P)) return DT_ERR_TOO_LARGE;
-    size_t nchunks = 0;
+    // the pointer and tensor tables must fit the fixed array (checked first:
+    // nothing below runs on a request that cannot be served)
+    if (n_tensors > kStaticScratchBytes / (P * sizeof(void *) + sizeof(dt::BucketTensor)))
+        return DT_ERR_TOO_LARGE;
     for (size_t t = 0; t < n_tensors; ++t) {
         if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
-        nchunks += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
         for (int p = 0; p < P && counts[t]; ++p)
             if (!grads[t * P + p]) return DT_ERR_INVALID;
     }
-    const size_t ptr_bytes = n_tensors * P * sizeof(void *);
-    if (nchunks > (kStaticScratchBytes - ptr_bytes) / sizeof(dt::BucketChunk)) return DT_ERR_TOO_LARGE;
-    if (nchunks == 0) return DT_OK;
 
     // no two gradient buffers may overlap: quadratic check, no allocation
     for (size_t t = 0; t < n_tensors; ++t)
@@ -98,26 +95,67 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     std::lock_guard<std::mutex> lock(g_static_mu);
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return DT_ERR_CUDA;
+
+    // plan: [T * P pointers][T tensor entries][block starts of every bucket];
+    // buckets are consecutive tensors, greedy in order under the cap (the
+    // rule of dt_bucket_plan).  Sizes are checked against the fixed array as
+    // the plan grows, before anything is enqueued.
+    const size_t ptr_bytes = n_tensors * P * sizeof(void *);
+    const size_t tab_bytes = n_tensors * sizeof(dt::BucketTensor);
+    if (ptr_bytes + tab_bytes > kStaticScratchBytes) return DT_ERR_TOO_LARGE;
+    memcpy(h_bucket_staging, grads, ptr_bytes);
+    dt::BucketTensor *tab = reinterpret_cast<dt::BucketTensor *>(h_bucket_staging + ptr_bytes);
+    uint32_t *starts = reinterpret_cast<uint32_t *>(h_bucket_staging + ptr_bytes + tab_bytes);
+    const size_t max_starts = (kStaticScratchBytes - ptr_bytes - tab_bytes) / sizeof(uint32_t);
+
+    struct Launch {
+        size_t tb, te, start_off;
+        uint64_t total, per_block;
+        uint32_t blocks;
+    };
+    static Launch launches[4096];   // buckets of this call (guarded by g_static_mu)
+    size_t nl = 0, n_starts = 0;
+    size_t t = 0;
+    while (t < n_tensors) {
+        // one bucket: [tb, te)
+        const size_t tb = t;
+        size_t filled = 0;
+        uint64_t first = 0;
+        while (t < n_tensors && !(filled > 0 && filled + counts[t] * es > cap)) {
+            bool al = true;
+            for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
+            tab[t].first = first;
+            tab[t].count = counts[t];
+            tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
+            tab[t].pad = 0;
+            first += dt::bucket_padded(counts[t], dtype);
+            filled += counts[t] * es;
+            ++t;
+        }
+        if (first == 0) continue;   // only empty tensors
+        if (nl == sizeof(launches) / sizeof(launches[0])) return DT_ERR_TOO_LARGE;
+        Launch &L = launches[nl++];
+        L.tb = tb;
+        L.te = t;
+        L.total = first;
+        if (dt::bucket_grid(dtype, op, P, L.total, device, &L.blocks, &L.per_block) != cudaSuccess)
+            return DT_ERR_CUDA;
+        if (n_starts + L.blocks > max_starts) return DT_ERR_TOO_LARGE;
+        L.start_off = n_starts;
+        size_t k = L.tb;
+        for (uint32_t j = 0; j < L.blocks; ++j) {
+            const uint64_t lo = (uint64_t)j * L.per_block;
+            while (k + 1 < L.te && tab[k + 1].first <= lo) ++k;
+            starts[n_starts++] = (uint32_t)(k - L.tb);
+        }
+    }
+    if (nl == 0) return DT_OK;
+
     void *scratch = nullptr;
     if (scratch_address(device, &scratch) != cudaSuccess) return DT_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    // plan: [T * P pointers][chunks in tensor order]; buckets are consecutive
-    // tensors, greedy in order under the cap, as in dt_bucket_plan
-    memcpy(h_bucket_staging, grads, ptr_bytes);
-    dt::BucketChunk *chunks = reinterpret_cast<dt::BucketChunk *>(h_bucket_staging + ptr_bytes);
-    size_t c = 0;
-    for (size_t t = 0; t < n_tensors; ++t) {
-        bool al = true;
-        for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
-        for (size_t beg = 0; beg < counts[t]; beg += dt::kBucketChunkElems) {
-            chunks[c].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
-            chunks[c].nelem = (uint32_t)std::min<size_t>(dt::kBucketChunkElems, counts[t] - beg);
-            chunks[c].begin = beg;
-            ++c;
-        }
-    }
-    cudaError_t e = cudaMemcpyAsync(scratch, h_bucket_staging, ptr_bytes + c * sizeof(dt::BucketChunk),
+    cudaError_t e = cudaMemcpyAsync(scratch, h_bucket_staging,
+                                    ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t),
                                     cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return DT_ERR_CUDA;
 
@@ -129,22 +167,14 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     bp.avg_scale = bp.avg_pow2 ? 1.0f / (float)P : 0.0f;
     // one launch per bucket, no signal barrier between buckets: with no group
     // there is no window, and stream order already orders the buckets
-    size_t first = 0, filled = 0;
-    c = 0;
-    for (size_t t = 0; t <= n_tensors; ++t) {
-        const bool close = t == n_tensors ||
-                           (filled > 0 && filled + counts[t] * es > cap);
-        if (close && c > first) {
-            bp.chunks = reinterpret_cast<const dt::BucketChunk *>(d + ptr_bytes) + first;
-            bp.nchunks = (uint32_t)(c - first);
-            e = dt::launch_bucket(bp, dtype, op, device, s);
-            if (e != cudaSuccess) return DT_ERR_CUDA;
-            first = c;
-        }
-        if (close) filled = 0;
-        if (t == n_tensors) break;
-        filled += counts[t] * es;
-        c += (counts[t] + dt::kBucketChunkElems - 1) / dt::kBucketChunkElems;
+    for (size_t i = 0; i < nl; ++i) {
+        const Launch &L = launches[i];
+        bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
+        bp.block_start = reinterpret_cast<const uint32_t *>(d + ptr_bytes + tab_bytes) + L.start_off;
+        bp.ntensors = (uint32_t)(L.te - L.tb);
+        bp.total = L.total;
+        bp.per_block = L.per_block;
+        if (dt::launch_bucket(bp, dtype, op, device, s) != cudaSuccess) return DT_ERR_CUDA;
     }
     return DT_OK;
 }

@@ -65,11 +65,23 @@ def test_static_bucket_allreduce_matches_group_version_two_calls(dt):
 
 
 def test_static_bucket_allreduce_rejects_tables_past_the_fixed_array(dt):
-    P = 4
-    counts = [1 << 31] * 16            # 16 x 65536 chunks: far past the 1 MiB array
-    fake = [[(t * P + p + 1) << 40 for p in range(P)] for t in range(len(counts))]
+    # Every pointer below is real, distinct device memory, so the check is
+    # exercised without ever handing a kernel an address it may not touch.
+    P = 16
+    T = 8200                      # 8200 * 16 pointers * 8 B > 1 MiB of pointer table
+    buf = torch.zeros(T * P * 8, dtype=torch.bfloat16, device="cuda")
+    base = buf.data_ptr()
+    grads = [[base + (t * P + p) * 16 for p in range(P)] for t in range(T)]
     n0 = dt.dt_launch_count()
     with pytest.raises(dt.DtError) as e:
-        dt.dt_bucket_allreduce_static(P, fake, counts, "bf16", "avg")
+        dt.dt_bucket_allreduce_static(P, grads, [1] * T, "bf16", "avg")
+    assert e.value.status == dt.DT_ERR_TOO_LARGE
+    # more buckets than the fixed launch list holds: one tensor per bucket
+    T = 5000
+    grads = [[base + (t * 2 + p) * 16 for p in range(2)] for t in range(T)]
+    with pytest.raises(dt.DtError) as e:
+        dt.dt_bucket_allreduce_static(2, grads, [1] * T, "bf16", "sum", bucket_cap_bytes=1)
     assert e.value.status == dt.DT_ERR_TOO_LARGE
     assert dt.dt_launch_count() == n0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(buf).item() == 0
