@@ -183,7 +183,7 @@ dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_byt
 /* Signal-window barrier: "Barrier：仅信号（Signals Only）".  The group keeps
  * an int32 window win[P][P] in HBM (row r of rank q's window is win[q][r]).
  * The g-th barrier (1-based generation, bumped by every call) is one kernel
- * with one thread block per rank: rank r adds 1 (AtomicAdd, release) to
+ * in which each rank is one warp: rank r adds 1 (AtomicAdd, release) to
  * win[q][r] of every peer q != r, then waits until win[r][s] >= g (Ge,
  * acquire) for every s != r.  Afterwards win[r][s] == g for s != r and
  * win[r][r] == 0.  Each wait gives up after the group's time limit and

@@ -10,14 +10,16 @@
 // window raises the threshold: the g-th barrier waits for g.
 //
 // Here the window is int32 win[P][P] in HBM (win[q][r] is row r of rank q's
-// window) and the ranks are the P blocks of one cooperative launch, so all of
-// them are resident together.  Lane q of block r's first warp notifies peer
-// q with a release reduction and then polls row q of rank r's window with
-// acquire loads.  The generation is kept per rank on the device (rank_gen),
-// so a captured and replayed launch still raises the threshold each time.
-// Every poll loop ends after the group's time limit (or an iteration bound);
-// a rank that gives up records DT_ERR_TIMEOUT once in the error word and its
-// host-mapped mirror and returns, so the GPU is never held.
+// window).  In the stand-alone barrier each rank is one warp of a single
+// block (warps of one block are always resident together, so the ranks can
+// wait on each other without a cooperative launch); in the ordering test
+// each rank is a block of a cooperative launch.  Lane q of rank r's warp
+// notifies peer q with a release reduction and then polls row q of rank r's
+// window with acquire loads.  The generation is kept per rank on the device
+// (rank_gen), so a captured and replayed launch still raises the threshold
+// each time.  Every poll loop ends after the group's time limit (or an
+// iteration bound); a rank that gives up records DT_ERR_TIMEOUT once in the
+// error word and its host-mapped mirror and returns, so the GPU is never held.
 #include "dt_internal.h"
 #include "dt_device.cuh"
 
@@ -78,10 +80,11 @@ __device__ bool rank_barrier(const BarrierParams &p, int r)
     return bad == 0;
 }
 
-__global__ void __launch_bounds__(32) barrier_kernel(const __grid_constant__ BarrierParams p)
+// One block of 32 * P threads: warp r is rank r.
+__global__ void __launch_bounds__(32 * DT_MAX_RANKS) barrier_kernel(const __grid_constant__ BarrierParams p)
 {
     pdl_begin();
-    rank_barrier<false>(p, blockIdx.x);
+    rank_barrier<false>(p, threadIdx.x >> 5);
 }
 
 __device__ void copy_bytes(unsigned char *dst, const unsigned char *src, uint64_t n)
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ 
 
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s)
 {
-    return launch_kernel(barrier_kernel, dim3(p.P), dim3(32), 0, s, true, p);
+    return launch_kernel(barrier_kernel, dim3(1), dim3(32 * p.P), 0, s, false, p);
 }
 
 cudaError_t launch_ring(const RingParams &p, cudaStream_t s)

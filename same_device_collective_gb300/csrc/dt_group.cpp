@@ -587,100 +587,116 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     const size_t es = elem_bytes(dtype);
     const size_t cap = bucket_cap_bytes ? bucket_cap_bytes : DT_DEFAULT_BUCKET_CAP_BYTES;
 
-    // validate and find overlapping gradient buffers (sorted sweep)
-    std::vector<Range> ranges;
-    ranges.reserve(n_tensors * P);
-    for (size_t t = 0; t < n_tensors; ++t) {
-        if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
-        if (counts[t] == 0) continue;
-        for (int p = 0; p < P; ++p) {
-            const void *ptr = grads[t * P + p];
-            if (!ptr) return DT_ERR_INVALID;
-            ranges.push_back({(uintptr_t)ptr, (uintptr_t)ptr + counts[t] * es, p, 1});
-        }
-    }
-    if (ranges.empty()) return DT_OK;
-    std::sort(ranges.begin(), ranges.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
-    for (size_t i = 1; i < ranges.size(); ++i)
-        if (ranges[i].lo < ranges[i - 1].hi) return DT_ERR_INVALID;
+    // the call's arguments, as the key of a cached plan
+    std::vector<uint64_t> key;
+    key.reserve(4 + n_tensors * (P + 1));
+    key.push_back((uint64_t)dtype);
+    key.push_back((uint64_t)op);
+    key.push_back((uint64_t)cap);
+    key.push_back((uint64_t)n_tensors);
+    for (size_t t = 0; t < n_tensors; ++t) key.push_back((uint64_t)counts[t]);
+    for (size_t i = 0; i < n_tensors * P; ++i) key.push_back((uint64_t)(uintptr_t)grads[i]);
 
-    std::vector<size_t> bucket_of(n_tensors);
-    const size_t nb = plan_buckets(counts, n_tensors, es, cap, bucket_of.data());
+    int k = -1;
+    for (int j = 0; j < dt_group::kPlanSlots; ++j)
+        if (g->plan_used[j] && g->plan_key[j] == key) k = j;
 
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    // per bucket: its tensors [tb, te), padded size, grid and slice length
-    struct BucketLaunch {
-        size_t tb, te;
-        uint64_t total, per_block;
-        uint32_t blocks;
-        size_t start_off;   // index of its first block_start entry
-    };
-    std::vector<BucketLaunch> bl(nb);
-    size_t n_starts = 0;
-    for (size_t b = 0, t = 0; b < nb; ++b) {
-        BucketLaunch &L = bl[b];
-        L.tb = t;
-        L.total = 0;
-        while (t < n_tensors && bucket_of[t] == b) L.total += dt::bucket_padded(counts[t++], dtype);
-        L.te = t;
-        L.blocks = 0;
-        L.per_block = 1;
-        if (L.total) {
-            cudaError_t e = dt::bucket_grid(dtype, op, P, L.total, g->device, &L.blocks, &L.per_block);
-            if (e != cudaSuccess) return cuda_status(e);
-        }
-        L.start_off = n_starts;
-        n_starts += L.blocks;
-    }
-
-    // plan layout: [T * P pointers][T tensor entries][block starts]
-    const size_t ptr_bytes = n_tensors * P * sizeof(void *);
-    const size_t tab_bytes = n_tensors * sizeof(dt::BucketTensor);
-    const size_t plan_bytes = ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t);
-    const int k = g->next_plan;
-    g->next_plan = (k + 1) % dt_group::kPlanSlots;
     cudaError_t e = cudaSuccess;
-    if (g->plan_used[k]) e = cudaEventSynchronize(g->plan_done[k]);
-    if (e == cudaSuccess) e = grow_plan_slot(g, k, plan_bytes);
-    if (e != cudaSuccess) return cuda_status(e);
 
-    unsigned char *h = static_cast<unsigned char *>(g->h_plan[k]);
-    memcpy(h, grads, ptr_bytes);
-    dt::BucketTensor *tab = reinterpret_cast<dt::BucketTensor *>(h + ptr_bytes);
-    uint32_t *starts = reinterpret_cast<uint32_t *>(h + ptr_bytes + tab_bytes);
-    for (const BucketLaunch &L : bl) {
-        uint64_t first = 0;
-        for (size_t t = L.tb; t < L.te; ++t) {
-            bool al = true;
-            for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
-            tab[t].first = first;
-            tab[t].count = counts[t];
-            tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
-            tab[t].pad = 0;
-            first += dt::bucket_padded(counts[t], dtype);
+    if (k < 0) {
+        // validate and find overlapping gradient buffers (sorted sweep)
+        std::vector<Range> ranges;
+        ranges.reserve(n_tensors * P);
+        for (size_t t = 0; t < n_tensors; ++t) {
+            if (counts[t] > SIZE_MAX / 16) return DT_ERR_INVALID;
+            if (counts[t] == 0) continue;
+            for (int p = 0; p < P; ++p) {
+                const void *ptr = grads[t * P + p];
+                if (!ptr) return DT_ERR_INVALID;
+                ranges.push_back({(uintptr_t)ptr, (uintptr_t)ptr + counts[t] * es, p, 1});
+            }
         }
-        // block j starts at the last tensor (bucket-relative) with first <= j * per_block
-        size_t t = L.tb;
-        for (uint32_t j = 0; j < L.blocks; ++j) {
-            const uint64_t lo = (uint64_t)j * L.per_block;
-            while (t + 1 < L.te && tab[t + 1].first <= lo) ++t;
-            starts[L.start_off + j] = (uint32_t)(t - L.tb);
+        if (ranges.empty()) return DT_OK;
+        std::sort(ranges.begin(), ranges.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
+        for (size_t i = 1; i < ranges.size(); ++i)
+            if (ranges[i].lo < ranges[i - 1].hi) return DT_ERR_INVALID;
+
+        std::vector<size_t> bucket_of(n_tensors);
+        const size_t nb = plan_buckets(counts, n_tensors, es, cap, bucket_of.data());
+
+        // per bucket: its tensors [tb, te), padded size, grid and slice length
+        std::vector<dt_group::PlanLaunch> bl(nb);
+        size_t n_starts = 0;
+        for (size_t b = 0, t = 0; b < nb; ++b) {
+            dt_group::PlanLaunch &L = bl[b];
+            L.tb = t;
+            L.total = 0;
+            while (t < n_tensors && bucket_of[t] == b) L.total += dt::bucket_padded(counts[t++], dtype);
+            L.te = t;
+            L.blocks = 0;
+            L.per_block = 1;
+            if (L.total) {
+                e = dt::bucket_grid(dtype, op, P, L.total, g->device, &L.blocks, &L.per_block);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
+            L.start_off = n_starts;
+            n_starts += L.blocks;
         }
+
+        // plan layout: [T * P pointers][T tensor entries][block starts]
+        const size_t ptr_bytes = n_tensors * P * sizeof(void *);
+        const size_t tab_bytes = n_tensors * sizeof(dt::BucketTensor);
+        const size_t plan_bytes = ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t);
+        k = g->next_plan;
+        g->next_plan = (k + 1) % dt_group::kPlanSlots;
+        if (g->plan_used[k]) e = cudaEventSynchronize(g->plan_done[k]);
+        g->plan_key[k].clear();   // the slot no longer holds a valid plan
+        if (e == cudaSuccess) e = grow_plan_slot(g, k, plan_bytes);
+        if (e != cudaSuccess) return cuda_status(e);
+
+        unsigned char *h = static_cast<unsigned char *>(g->h_plan[k]);
+        memcpy(h, grads, ptr_bytes);
+        dt::BucketTensor *tab = reinterpret_cast<dt::BucketTensor *>(h + ptr_bytes);
+        uint32_t *starts = reinterpret_cast<uint32_t *>(h + ptr_bytes + tab_bytes);
+        for (const dt_group::PlanLaunch &L : bl) {
+            uint64_t first = 0;
+            for (size_t t = L.tb; t < L.te; ++t) {
+                bool al = true;
+                for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
+                tab[t].first = first;
+                tab[t].count = counts[t];
+                tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
+                tab[t].pad = 0;
+                first += dt::bucket_padded(counts[t], dtype);
+            }
+            // block j starts at the last tensor (bucket-relative) with first <= j * per_block
+            size_t t = L.tb;
+            for (uint32_t j = 0; j < L.blocks; ++j) {
+                const uint64_t lo = (uint64_t)j * L.per_block;
+                while (t + 1 < L.te && tab[t + 1].first <= lo) ++t;
+                starts[L.start_off + j] = (uint32_t)(t - L.tb);
+            }
+        }
+        e = cudaMemcpyAsync(g->d_plan[k], h, plan_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        g->plan_key[k] = std::move(key);
+        g->plan_launches[k] = std::move(bl);
+        g->plan_ptr_bytes[k] = ptr_bytes;
+        g->plan_tab_bytes[k] = tab_bytes;
     }
 
-    e = cudaMemcpyAsync(g->d_plan[k], h, plan_bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_status(e);
     const unsigned char *d = static_cast<const unsigned char *>(g->d_plan[k]);
-
+    const size_t ptr_bytes = g->plan_ptr_bytes[k], tab_bytes = g->plan_tab_bytes[k];
+    const std::vector<dt_group::PlanLaunch> &bl = g->plan_launches[k];
     dt::BucketParams bp;
     bp.ptrs = reinterpret_cast<void *const *>(d);
     bp.P = P;
     set_avg(P, &bp.avg_scale, &bp.avg_pow2);
-    for (size_t b = 0; b < nb; ++b) {
-        const BucketLaunch &L = bl[b];
+    for (size_t b = 0; b < bl.size(); ++b) {
+        const dt_group::PlanLaunch &L = bl[b];
         bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
         bp.block_start = reinterpret_cast<const uint32_t *>(d + ptr_bytes + tab_bytes) + L.start_off;
         bp.ntensors = (uint32_t)(L.te - L.tb);
@@ -688,7 +704,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         bp.per_block = L.per_block;
         e = dt::launch_bucket(bp, dtype, op, g->device, s);
         if (e != cudaSuccess) break;
-        if (b + 1 < nb) {
+        if (b + 1 < bl.size()) {
             st = issue_barrier(g, s);
             if (st != DT_OK) return st;
         }

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "dt.h"
 
@@ -186,14 +187,26 @@ struct dt_group {
     dt::DevError *h_err = nullptr;   // host-mapped mirror (host view)
     dt::DevError *h_err_dev = nullptr;
 
-    // bucket plan staging: kPlanSlots pinned host buffers and device buffers,
-    // each reused only after its event says the last kernel reading it ended
+    // bucket plans: kPlanSlots pinned host buffers and device buffers.  A slot
+    // keeps the arguments its plan was built for (plan_key) and the launches
+    // it describes, so a call with the same gradients, counts, dtype, op and
+    // cap reuses the uploaded plan; a slot is rebuilt only after its event
+    // says the last kernel reading it ended.
+    struct PlanLaunch {
+        size_t tb, te, start_off;
+        uint64_t total, per_block;
+        uint32_t blocks;
+    };
     static constexpr int kPlanSlots = 2;
     void *h_plan[kPlanSlots] = {nullptr, nullptr};
     void *d_plan[kPlanSlots] = {nullptr, nullptr};
     size_t plan_bytes[kPlanSlots] = {0, 0};
     cudaEvent_t plan_done[kPlanSlots] = {nullptr, nullptr};
     bool plan_used[kPlanSlots] = {false, false};
+    std::vector<uint64_t> plan_key[kPlanSlots];
+    std::vector<PlanLaunch> plan_launches[kPlanSlots];
+    size_t plan_ptr_bytes[kPlanSlots] = {0, 0};
+    size_t plan_tab_bytes[kPlanSlots] = {0, 0};
     int next_plan = 0;
 
     std::mutex mu;

@@ -111,17 +111,19 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
                 }
                 o[k] = pack_bf16x2(lo, hi);
             } else {
-                uint32_t blo = w[0][k] & 0xFFFFu, bhi = w[0][k] >> 16;
+                // the running choice is kept as the widened fp32 value; a select
+                // moves bits unchanged, so the chosen bf16 element (NaN payload
+                // included) is recovered from those bits by a shift
                 float flo = bf16_lo(w[0][k]), fhi = bf16_hi(w[0][k]);
 #pragma unroll
                 for (int r = 1; r < PMAX; ++r) {
                     if (r < P) {
                         const float xl = bf16_lo(w[r][k]), xh = bf16_hi(w[r][k]);
-                        if (take_f<OP>(xl, flo)) { flo = xl; blo = w[r][k] & 0xFFFFu; }
-                        if (take_f<OP>(xh, fhi)) { fhi = xh; bhi = w[r][k] >> 16; }
+                        flo = take_f<OP>(xl, flo) ? xl : flo;
+                        fhi = take_f<OP>(xh, fhi) ? xh : fhi;
                     }
                 }
-                o[k] = blo | (bhi << 16);
+                o[k] = (__float_as_uint(flo) >> 16) | (__float_as_uint(fhi) & 0xFFFF0000u);
             }
         }
     }
@@ -151,17 +153,18 @@ __device__ __forceinline__ void reduce_elem(const void *const *base, uint64_t in
         if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
         for (int k = 0; k < ndst; ++k) static_cast<float *>(dst[k])[i] = acc;
     } else {
-        uint16_t b = static_cast<const uint16_t *>(base[0])[j];
-        float acc = bf16_to_f32(b);
+        float acc = bf16_to_f32(static_cast<const uint16_t *>(base[0])[j]);
         for (int r = 1; r < P; ++r) {
-            const uint16_t xb = static_cast<const uint16_t *>(base[r])[j];
-            const float x = bf16_to_f32(xb);
+            const float x = bf16_to_f32(static_cast<const uint16_t *>(base[r])[j]);
             if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x);
-            else if (take_f<OP>(x, acc)) { acc = x; b = xb; }
+            else acc = take_f<OP>(x, acc) ? x : acc;
         }
+        uint16_t b;
         if constexpr (OP == DT_SUM || OP == DT_AVG) {
             if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
             b = f32_to_bf16(acc);
+        } else {
+            b = (uint16_t)(__float_as_uint(acc) >> 16);   // the chosen element's bits
         }
         for (int k = 0; k < ndst; ++k) static_cast<uint16_t *>(dst[k])[i] = b;
     }

@@ -250,6 +250,28 @@ def test_bucket_allreduce_matches_oracle(dt, dtype, op, P):
         assert np.array_equal(win, oracle.expected_window(P, nb - 1)), f"cap={cap}"
 
 
+def test_bucket_plan_reuse_across_calls(dt):
+    # Two gradient sets used in turn: each call either reuses a cached plan
+    # (same gradients, counts, dtype, op and cap) or rebuilds a slot.
+    P = 4
+    rng = np.random.default_rng(77)
+    sets = {}
+    for name, counts in (("A", [100, 40_000, 7]), ("B", [3000, 5, 70_000, 1])):
+        grads = [[torch.from_numpy(rng.standard_normal(c).astype(np.float32) * 1e-3)
+                  .to(torch.bfloat16).cuda() for _ in range(P)] for c in counts]
+        sets[name] = (counts, grads, [[host(x).copy() for x in row] for row in grads])
+    with group(P) as g:
+        for name in ["A", "B", "A", "B", "A", "A"]:
+            counts, grads, ref = sets[name]
+            dt.dt_bucket_allreduce(g, grads, counts, "bf16", "sum", bucket_cap_bytes=64 << 10)
+            oracle.bucket_allreduce("bf16", "sum", ref)
+            torch.cuda.synchronize()
+            for t in range(len(counts)):
+                for p in range(P):
+                    assert_same(host(grads[t][p]), ref[t][p], f"{name} tensor {t} rank {p}")
+        assert dt.dt_group_check(g) == dt.DT_OK
+
+
 def test_bucket_plan_matches_oracle_plan(dt):
     from same_device_collective_gb300 import workloads
     counts = workloads.bucket_counts()
