@@ -13,8 +13,23 @@
  *
  * Group-wide calls.  One call carries every rank's buffer (rank ==
  * DT_ALL_RANKS, pointer arrays with P entries) and runs as one kernel that
- * reads all P rank buffers directly from HBM.  Per-rank calls (rank >= 0, one
- * host thread per rank) are reserved and return DT_ERR_UNSUPPORTED.
+ * reads all P rank buffers directly from HBM.
+ *
+ * Rank-local calls.  As in DTorch, where every rank is a host thread that
+ * calls ThreadGroup with its own tensor, each of P threads may call with
+ * rank = its rank (0..P-1), one-entry pointer arrays and its own stream.  The
+ * ranks meet on the host the way the MemoryTensorStore of §3.4 does (mutex,
+ * condition variable, CUDA events): each rank records a ready event on its
+ * stream, the last rank to arrive makes its stream wait on the others' ready
+ * events and launches the one group-wide kernel, and every other rank's
+ * stream waits on that launch's done event, so results are valid in each
+ * rank's own stream order.  All ranks of a round must make the same call
+ * (same collective, sizes, dtype, op, flags; AllGather's rows are each
+ * rank's own) or every rank gets DT_ERR_INVALID.  A rank whose partners do
+ * not all arrive within the group's time limit gets DT_ERR_TIMEOUT and the
+ * group is poisoned until dt_group_reset.  Ranks of one group must not mix
+ * rank-local and group-wide calls within a round.  dt_bucket_allreduce is
+ * group-wide only.
  *
  * Conventions shared by every entry point:
  *   Streams   `stream` is a cudaStream_t passed as void* (NULL = the legacy
@@ -141,7 +156,8 @@ dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void 
 
 /* AllGather (S(0) -> R): "集合通信组件" §2.1 AllGatherIntoTensor (equal
  * shards, rows == NULL: every rank has rows_equal rows) and AllGather with
- * uneven shards (rows[r] rows on rank r).  Rows are row_bytes bytes; rank r's
+ * uneven shards (rows[r] rows on rank r).  In a rank-local call rows must be
+ * NULL and rows_equal is the calling rank's own row count.  Rows are row_bytes bytes; rank r's
  * rows land at row offset rows[0] + ... + rows[r-1] of every out[q], which
  * holds the sum of all rows.  With DT_SHARED_OUTPUT every out[] is one buffer
  * written once.  Byte copies: any element type. */

@@ -10,6 +10,7 @@
 // kernel's parameter block (or, for buckets, as a table staged in HBM), and
 // ordering is the order of the caller's stream.
 #include <algorithm>
+#include <chrono>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -127,9 +128,8 @@ dt_status cuda_status(cudaError_t e)
 
 dt_status check_rank(dt_group *g, int rank)
 {
-    if (rank == DT_ALL_RANKS) return DT_OK;
-    if (rank >= 0 && rank < g->P) return DT_ERR_UNSUPPORTED;   // per-rank calls: reserved
-    return DT_ERR_INVALID;
+    (void)g;
+    return rank == DT_ALL_RANKS ? DT_OK : DT_ERR_INVALID;   // rank-local calls go elsewhere
 }
 
 bool is_pow2(int P) { return P > 0 && (P & (P - 1)) == 0; }
@@ -179,6 +179,10 @@ void destroy_all(dt_group *g)
         release_plan_slot(g, k);
         if (g->plan_done[k]) cudaEventDestroy(g->plan_done[k]);
     }
+    for (int r = 0; r < DT_MAX_RANKS; ++r)
+        if (g->rv_ready[r]) cudaEventDestroy(g->rv_ready[r]);
+    for (int k = 0; k < 2; ++k)
+        if (g->rv_done[k]) cudaEventDestroy(g->rv_done[k]);
     if (g->d_win) cudaFree(g->d_win);
     if (g->d_err) cudaFree(g->d_err);
     if (g->h_err) cudaFreeHost(g->h_err);
@@ -209,6 +213,134 @@ size_t plan_buckets(const size_t *counts, size_t T, size_t es, size_t cap, size_
         filled += bytes;
     }
     return T ? b + 1 : 0;
+}
+
+enum CallKind { CK_ALLREDUCE = 1, CK_REDUCE_SCATTER, CK_ALL_GATHER, CK_ALL_TO_ALL, CK_BARRIER };
+
+bool same_call(const dt_group::RankCall &a, const dt_group::RankCall &b)
+{
+    // every rank of a round must make the same call; an uneven AllGather's
+    // row counts are each rank's own
+    return a.kind == b.kind && a.dtype == b.dtype && a.op == b.op && a.flags == b.flags &&
+           a.row_bytes == b.row_bytes && (a.kind == CK_ALL_GATHER || a.count == b.count);
+}
+
+// The last rank of a round launches the group-wide call on its own stream,
+// after that stream has waited for every other rank's inputs (their ready
+// events: the DestGet / StreamWaitEvent step of the TensorStore protocol).
+dt_status launch_round(dt_group *g, int last)
+{
+    const int P = g->P;
+    const dt_group::RankCall &c0 = g->rv_call[0];
+    for (int r = 1; r < P; ++r)
+        if (!same_call(g->rv_call[r], c0)) return DT_ERR_INVALID;
+    cudaStream_t s = g->rv_call[last].stream;
+    for (int r = 0; r < P; ++r)
+        if (r != last && cudaStreamWaitEvent(s, g->rv_ready[r], 0) != cudaSuccess) return DT_ERR_CUDA;
+    const void *ins[DT_MAX_RANKS];
+    void *outs[DT_MAX_RANKS];
+    size_t rows[DT_MAX_RANKS];
+    for (int r = 0; r < P; ++r) {
+        ins[r] = g->rv_call[r].in;
+        outs[r] = g->rv_call[r].out;
+        rows[r] = g->rv_call[r].count;
+    }
+    switch (c0.kind) {
+    case CK_ALLREDUCE:
+        return dt_allreduce(g, DT_ALL_RANKS, ins, outs, c0.count, c0.dtype, c0.op, c0.flags, s);
+    case CK_REDUCE_SCATTER:
+        return dt_reduce_scatter(g, DT_ALL_RANKS, ins, outs, c0.count, c0.dtype, c0.op, s);
+    case CK_ALL_GATHER:
+        return dt_all_gather(g, DT_ALL_RANKS, ins, outs, rows, 0, c0.row_bytes, c0.flags, s);
+    case CK_ALL_TO_ALL:
+        return dt_all_to_all(g, DT_ALL_RANKS, ins, outs, c0.count, s);
+    case CK_BARRIER:
+        return dt_barrier(g, DT_ALL_RANKS, s);
+    }
+    return DT_ERR_INVALID;
+}
+
+void poison(dt_group *g, dt_status code)
+{
+    std::lock_guard<std::mutex> lock(g->mu);
+    if (!g->poisoned) {
+        g->poisoned = true;
+        g->poison_code = code;
+    }
+}
+
+// One rank's part of a rank-local call.  The rank records a ready event on its
+// stream (SrcSet), then meets the other ranks.  All but the last wait, at most
+// the group's time limit, for the round to complete and then make their
+// stream wait on the round's done event; the last launches for everyone.  A
+// wait that runs out abandons the round: every rank of it returns
+// DT_ERR_TIMEOUT and the group is poisoned until dt_group_reset.
+dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
+{
+    if (rank < 0 || rank >= g->P) return DT_ERR_INVALID;
+    {
+        std::lock_guard<std::mutex> lock(g->mu);
+        dt_status st = take_device_error(g);
+        if (st != DT_OK) return st;
+    }
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    if (cudaEventRecord(g->rv_ready[rank], call.stream) != cudaSuccess) return DT_ERR_CUDA;
+
+    std::unique_lock<std::mutex> lk(g->rv_mu);
+    if (g->rv_aborted) return DT_ERR_POISONED;
+    if (g->rv_present[rank]) return DT_ERR_INVALID;   // this rank is already in the round
+    g->rv_call[rank] = call;
+    g->rv_present[rank] = true;
+    const uint64_t my_round = g->rv_round;
+    const int slot = (int)(my_round & 1);
+
+    if (++g->rv_arrived < g->P) {
+        const auto deadline = std::chrono::steady_clock::now() +
+                              std::chrono::milliseconds(g->timeout_ms);
+        g->rv_cv.wait_until(lk, deadline, [&] { return g->rv_round != my_round || g->rv_aborted; });
+        if (g->rv_round != my_round) {
+            dt_status st = g->rv_status[slot];
+            cudaEvent_t done = g->rv_done[slot];
+            lk.unlock();
+            if (st == DT_OK && cudaStreamWaitEvent(call.stream, done, 0) != cudaSuccess)
+                st = DT_ERR_CUDA;
+            return st;
+        }
+        g->rv_aborted = true;
+        g->rv_present[rank] = false;
+        --g->rv_arrived;
+        lk.unlock();
+        g->rv_cv.notify_all();
+        poison(g, DT_ERR_TIMEOUT);
+        return DT_ERR_TIMEOUT;
+    }
+
+    dt_status st = launch_round(g, rank);
+    if (st == DT_OK && cudaEventRecord(g->rv_done[slot], call.stream) != cudaSuccess) st = DT_ERR_CUDA;
+    g->rv_status[slot] = st;
+    for (int r = 0; r < DT_MAX_RANKS; ++r) g->rv_present[r] = false;
+    g->rv_arrived = 0;
+    ++g->rv_round;
+    lk.unlock();
+    g->rv_cv.notify_all();
+    return st;
+}
+
+dt_group::RankCall make_call(int kind, const void *const *in, void *const *out, size_t count,
+                             size_t row_bytes, int dtype, int op, unsigned flags, void *stream)
+{
+    dt_group::RankCall c;
+    c.kind = kind;
+    c.in = in ? in[0] : nullptr;
+    c.out = out ? out[0] : nullptr;
+    c.count = count;
+    c.row_bytes = row_bytes;
+    c.dtype = dtype;
+    c.op = op;
+    c.flags = flags;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return c;
 }
 
 }  // namespace
@@ -265,6 +397,10 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
         e = cudaEventCreateWithFlags(&g->plan_done[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = grow_plan_slot(g, k, (size_t)1 << 20);
     }
+    for (int r = 0; r < world_size && e == cudaSuccess; ++r)
+        e = cudaEventCreateWithFlags(&g->rv_ready[r], cudaEventDisableTiming);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k)
+        e = cudaEventCreateWithFlags(&g->rv_done[k], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         destroy_all(g);
@@ -301,6 +437,14 @@ dt_status dt_group_reset(dt_group_t g, void *stream)
     g->poisoned = false;
     g->poison_code = DT_OK;
     g->barriers_issued = 0;
+    {
+        std::lock_guard<std::mutex> rv(g->rv_mu);
+        for (int r = 0; r < DT_MAX_RANKS; ++r) g->rv_present[r] = false;
+        g->rv_arrived = 0;
+        g->rv_aborted = false;
+        ++g->rv_round;
+    }
+    g->rv_cv.notify_all();
     return DT_OK;
 }
 
@@ -350,6 +494,10 @@ dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *cons
                        size_t count, int dtype, int op, unsigned flags, void *stream)
 {
     if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out) return DT_ERR_INVALID;
+        return rank_local(g, rank, make_call(CK_ALLREDUCE, in, out, count, 0, dtype, op, flags, stream));
+    }
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
     if (st != DT_OK) return st;
@@ -410,6 +558,11 @@ dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void 
                             size_t recv_count, int dtype, int op, void *stream)
 {
     if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out) return DT_ERR_INVALID;
+        return rank_local(g, rank, make_call(CK_REDUCE_SCATTER, in, out, recv_count, 0, dtype, op, 0,
+                                             stream));
+    }
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
     if (st != DT_OK) return st;
@@ -461,6 +614,12 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
                         void *stream)
 {
     if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        // a rank passes its own shard: rows must be NULL, rows_equal its row count
+        if (!in || !out || rows) return DT_ERR_INVALID;
+        return rank_local(g, rank, make_call(CK_ALL_GATHER, in, out, rows_equal, row_bytes, 0, 0,
+                                             flags, stream));
+    }
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
     if (st != DT_OK) return st;
@@ -524,6 +683,10 @@ dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *con
                         size_t chunk_bytes, void *stream)
 {
     if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out) return DT_ERR_INVALID;
+        return rank_local(g, rank, make_call(CK_ALL_TO_ALL, in, out, chunk_bytes, 0, 0, 0, 0, stream));
+    }
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
     if (st != DT_OK) return st;
@@ -718,6 +881,8 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
 dt_status dt_barrier(dt_group_t g, int rank, void *stream)
 {
     if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS)
+        return rank_local(g, rank, make_call(CK_BARRIER, nullptr, nullptr, 0, 0, 0, 0, 0, stream));
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
     if (st != DT_OK) return st;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <condition_variable>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -208,6 +209,30 @@ struct dt_group {
     size_t plan_ptr_bytes[kPlanSlots] = {0, 0};
     size_t plan_tab_bytes[kPlanSlots] = {0, 0};
     int next_plan = 0;
+
+    // rank-local calls: one host thread per rank meets the others here, like
+    // the MemoryTensorStore of the DTorch page (mutex, condition variable,
+    // CUDA events).  The last rank to arrive launches the group-wide kernel.
+    struct RankCall {
+        int kind;                 // which collective (dt_group.cpp: CallKind)
+        const void *in;
+        void *out;
+        size_t count;             // elements / recv_count / this rank's rows / chunk bytes
+        size_t row_bytes;
+        int dtype, op;
+        unsigned flags;
+        cudaStream_t stream;
+    };
+    std::mutex rv_mu;
+    std::condition_variable rv_cv;
+    RankCall rv_call[DT_MAX_RANKS];
+    bool rv_present[DT_MAX_RANKS] = {};
+    int rv_arrived = 0;
+    uint64_t rv_round = 0;
+    bool rv_aborted = false;
+    dt_status rv_status[2] = {DT_OK, DT_OK};
+    cudaEvent_t rv_ready[DT_MAX_RANKS] = {};
+    cudaEvent_t rv_done[2] = {nullptr, nullptr};
 
     std::mutex mu;
 };

@@ -374,7 +374,6 @@ def test_invalid_arguments_are_rejected_without_launch(dt):
         cases = [
             lambda: dt.dt_allreduce(g, dt.DT_ALL_RANKS, x, o, 64, "i32", "avg"),
             lambda: dt.dt_allreduce(g, 7, x, o, 64, "f32", "sum"),
-            lambda: dt.dt_allreduce(g, 0, x, o, 64, "f32", "sum"),
             lambda: dt.dt_allreduce(g, dt.DT_ALL_RANKS, x, [o[0], o[0], o[1]], 64, "f32", "sum"),
             lambda: dt.dt_allreduce(g, dt.DT_ALL_RANKS, x, [x[1], o[1], o[2]], 64, "f32", "sum"),
             lambda: dt.dt_allreduce(g, dt.DT_ALL_RANKS, x, o, 64, "f32", "sum", flags=0x4),

@@ -1,0 +1,176 @@
+"""Rank-local calls: P host threads, one per rank, each with its own buffers
+and its own CUDA stream, as DTorch drives ThreadGroup (one thread per rank,
+meeting through the MemoryTensorStore).  Results are compared bit for bit with
+the oracle; the host rendezvous's failure path (a rank that never arrives) is
+checked through its time limit, with no GPU fault."""
+from __future__ import annotations
+
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TORCH_DTYPE, bytes_of, group, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dt():
+    from same_device_collective_gb300 import dt as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+def run_ranks(P, fn):
+    """Run fn(rank) on P threads; returns the list of exceptions (None = ok)."""
+    errs = [None] * P
+
+    def body(r):
+        try:
+            fn(r)
+        except Exception as e:   # collected and checked by the caller
+            errs[r] = e
+
+    ts = [threading.Thread(target=body, args=(r,)) for r in range(P)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join(60)
+    assert not any(t.is_alive() for t in ts)
+    return errs
+
+
+def assert_same(got, want, what):
+    assert np.array_equal(bytes_of(got), bytes_of(want)), what
+
+
+@pytest.mark.parametrize("P", [2, 4, 8])
+@pytest.mark.parametrize("dtype,op", [("f32", "sum"), ("bf16", "avg"), ("i32", "max")])
+def test_rank_local_allreduce_and_reduce_scatter(dt, P, dtype, op):
+    n = 4096 * P + 8 * P
+    m = n // P
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    ins = [None] * P
+    outs = [None] * P
+    rss = [None] * P
+    with group(P) as g:
+        def rank(r):
+            s = streams[r]
+            with torch.cuda.stream(s):
+                gen = torch.Generator(device="cuda").manual_seed(1000 + r)
+                if dtype == "i32":
+                    x = torch.randint(-2 ** 20, 2 ** 20, (n,), generator=gen, device="cuda",
+                                      dtype=torch.int32)
+                else:
+                    x = (torch.rand(n, generator=gen, device="cuda") * 2 - 1).to(TORCH_DTYPE[dtype])
+                o = torch.empty_like(x)
+                rs = torch.empty(m, dtype=x.dtype, device="cuda")
+                # inputs were produced on this rank's stream just before the call
+                dt.dt_allreduce(g, r, [x], [o], n, dtype, op, 0, s)
+                dt.dt_reduce_scatter(g, r, [x], [rs], m, dtype, op, s)
+                ins[r], outs[r], rss[r] = x, o.clone(), rs.clone()   # read back in stream order
+        errs = run_ranks(P, rank)
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    hx = [host(x) for x in ins]
+    want = oracle.allreduce(dtype, op, hx)
+    for q in range(P):
+        assert_same(host(outs[q]), want[q], f"allreduce rank {q}")
+    want = oracle.reduce_scatter(dtype, op, hx)
+    for r in range(P):
+        assert_same(host(rss[r]), want[r], f"reduce_scatter rank {r}")
+
+
+@pytest.mark.parametrize("P", [2, 3, 8])
+def test_rank_local_uneven_all_gather_and_all_to_all(dt, P):
+    row_bytes = 64
+    rows = [3 + 5 * r for r in range(P)]
+    total = sum(rows)
+    chunk = 256
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    xs = [torch.randint(0, 256, (rows[r] * row_bytes,), dtype=torch.uint8, device="cuda")
+          for r in range(P)]
+    a2a_in = [torch.randint(0, 256, (P * chunk,), dtype=torch.uint8, device="cuda")
+              for _ in range(P)]
+    torch.cuda.synchronize()
+    ag = [torch.empty(total * row_bytes, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    a2a = [torch.empty(P * chunk, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    with group(P) as g:
+        def rank(r):
+            s = streams[r]
+            dt.dt_all_gather(g, r, [xs[r]], [ag[r]], None, rows[r], row_bytes, 0, s)
+            dt.dt_all_to_all(g, r, [a2a_in[r]], [a2a[r]], chunk, s)
+        errs = run_ranks(P, rank)
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+    want = oracle.all_gather_one([host(x) for x in xs], rows, row_bytes)
+    for q in range(P):
+        assert_same(host(ag[q]), want, f"all_gather rank {q}")
+    want = oracle.all_to_all([host(x) for x in a2a_in])
+    for j in range(P):
+        assert_same(host(a2a[j]), want[j], f"all_to_all rank {j}")
+
+
+@pytest.mark.parametrize("P", [2, 4, 16])
+def test_rank_local_barrier_window(dt, P):
+    G = 5
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    with group(P) as g:
+        def rank(r):
+            for _ in range(G):
+                dt.dt_barrier(g, r, streams[r])
+        errs = run_ranks(P, rank)
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+        assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, G))
+        assert dt.dt_group_check(g) == dt.DT_OK
+
+
+def test_rank_local_mismatched_calls_are_rejected(dt):
+    P = 3
+    xs = [torch.ones(64, device="cuda") for _ in range(P)]
+    os_ = [torch.empty(64, device="cuda") for _ in range(P)]
+    with group(P) as g:
+        n0 = dt.dt_launch_count()
+
+        def rank(r):
+            n = 64 if r != 1 else 32      # rank 1 disagrees on the size
+            dt.dt_allreduce(g, r, [xs[r]], [os_[r]], n, "f32", "sum", 0,
+                            torch.cuda.current_stream())
+        errs = run_ranks(P, rank)
+        assert all(isinstance(e, dt.DtError) and e.status == dt.DT_ERR_INVALID for e in errs)
+        assert dt.dt_launch_count() == n0
+        assert dt.dt_group_check(g) == dt.DT_OK
+
+
+def test_rank_local_missing_rank_times_out_and_reset_recovers(dt):
+    P = 4
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    with group(P) as g:
+        dt.dt_group_set_timeout_ms(g, 300)
+        n0 = dt.dt_launch_count()
+
+        def rank(r):
+            if r == 2:
+                return                       # this rank never arrives
+            dt.dt_barrier(g, r, streams[r])
+        errs = run_ranks(P, rank)
+        for r in range(P):
+            if r == 2:
+                assert errs[r] is None
+            else:
+                assert isinstance(errs[r], dt.DtError) and errs[r].status == dt.DT_ERR_TIMEOUT
+        assert dt.dt_launch_count() == n0   # nothing was launched
+        assert dt.dt_group_check(g) == dt.DT_ERR_TIMEOUT
+        with pytest.raises(dt.DtError):
+            dt.dt_barrier(g, 2, streams[2])  # the late rank finds the group poisoned
+        dt.dt_group_reset(g)
+        assert dt.dt_group_check(g) == dt.DT_OK
+        errs = run_ranks(P, lambda r: dt.dt_barrier(g, r, streams[r]))
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+        assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, 1))
