@@ -244,7 +244,7 @@ def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
 
 
 ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "uneven_all_gather",
-             "barrier"]
+             "barrier", "rank_local"]
 
 
 def measure_rows(dt, dev, peak, only=None):
@@ -388,6 +388,54 @@ def measure_rows(dt, dev, peak, only=None):
         rows["barrier_P16"] = {"us_per_call_stream": round(us_direct, 3),
                                "us_per_call_graph": us_graph if isinstance(us_graph, str)
                                else round(us_graph, 3), "calls": calls, "status_ok": win_ok}
+
+    # Rank-local mode: four host threads, one per rank, each with its own
+    # stream, drive the configured RS(avg) + AG step (barrier, RS, barrier,
+    # AG); every call meets on the host and the last rank launches.  Wall time
+    # of K steps after both ends are synchronised.
+    if want("rank_local"):
+        import threading
+        P, R, C = P_RANKS, ROWS, COLS
+        w = workloads.rs_ag(seed=1, P=P, rows=R, cols=C, device=str(dev))
+        xs = w.inputs
+        m = R // P * C
+        rs = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ag = [torch.empty(R, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        streams = [torch.cuda.Stream(dev) for _ in range(P)]
+        raws = [s_.cuda_stream for s_ in streams]
+        g = dt.dt_group_create(P, dev.index)
+
+        def rank_steps(r, k):
+            torch.cuda.set_device(dev)
+            for _ in range(k):
+                dt.dt_barrier(g, r, raws[r])
+                dt.dt_reduce_scatter(g, r, [xs[r]], [rs[r]], m, "bf16", "avg", raws[r])
+                dt.dt_barrier(g, r, raws[r])
+                dt.dt_all_gather(g, r, [rs[r]], [ag[r]], None, R // P, C * 2, 0, raws[r])
+
+        def run(k):
+            ts = [threading.Thread(target=rank_steps, args=(r, k)) for r in range(P)]
+            for t in ts:
+                t.start()
+            for t in ts:
+                t.join()
+
+        run(20)
+        torch.cuda.synchronize()
+        K = 500
+        t0 = time.perf_counter()
+        run(K)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        rs_b, ag_b = step_bytes()
+        gbs = (rs_b + ag_b) * K / el / 1e9
+        ok = dt.dt_group_check(g) == dt.DT_OK
+        dt.dt_group_destroy(g)
+        rows["rank_local_rs_ag_step_bf16_P4"] = {
+            "GB/s": round(gbs, 1), "us_per_step": round(el / K * 1e6, 2), "steps": K,
+            "frac_of_measured_hbm": round(gbs / peak, 4), "threads": P, "status_ok": ok,
+            "timing": "wall clock over K steps, both ends synchronised"}
+        del w, xs, rs, ag
 
     torch.cuda.empty_cache()
     return rows
