@@ -36,6 +36,10 @@
  *     one when it is strictly greater (smaller) or is a NaN, so a NaN
  *     propagates and ties (including +0 / -0) keep the lower rank's value.
  *     The selected element's original bits are the result.
+ *   - SUM_STEPWISE: the literal `result += DestGet(rank)` of [DT] §2.3, in
+ *     which every add lands in the tensor's own dtype: ranks in ascending
+ *     order, each fp32 add rounded back to bf16 before the next one.  For fp32
+ *     and int32 it is SUM.
  *   - Bucket plan: greedy in the given order; a bucket is closed when adding
  *     the next tensor would take it past the cap; a tensor larger than the
  *     cap gets a bucket of its own.
@@ -53,7 +57,7 @@
 #include <sched.h>
 
 enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_I32 = 2 };
-enum { ORC_SUM = 0, ORC_AVG = 1, ORC_MAX = 2, ORC_MIN = 3 };
+enum { ORC_SUM = 0, ORC_AVG = 1, ORC_MAX = 2, ORC_MIN = 3, ORC_SUM_STEPWISE = 4 };
 enum { ORC_OK = 0, ORC_INVALID = 1, ORC_UNSUPPORTED = 2 };
 
 #define ORC_MAX_RANKS 64
@@ -136,7 +140,7 @@ static int check_types(int dtype, int op)
 {
     if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_I32)
         return ORC_INVALID;
-    if (op < ORC_SUM || op > ORC_MIN)
+    if (op < ORC_SUM || op > ORC_SUM_STEPWISE)
         return ORC_INVALID;
     if (dtype == ORC_I32 && op == ORC_AVG)
         return ORC_UNSUPPORTED;
@@ -166,7 +170,7 @@ int orc_reduce(int dtype, int op, int P, const void *const *in, size_t in_offset
             int32_t acc = load_i(in[0], k);
             for (int r = 1; r < P; r++) {
                 int32_t x = load_i(in[r], k);
-                if (op == ORC_SUM)
+                if (op == ORC_SUM || op == ORC_SUM_STEPWISE)
                     acc = (int32_t)((uint32_t)acc + (uint32_t)x);   /* wraps mod 2^32 */
                 else if (op == ORC_MAX)
                     acc = x > acc ? x : acc;
@@ -188,6 +192,14 @@ int orc_reduce(int dtype, int op, int P, const void *const *in, size_t in_offset
             }
             size_t es = elem_size(dtype);
             memcpy((char *)out + es * i, (const char *)in[win] + es * k, es);
+        } else if (op == ORC_SUM_STEPWISE) {
+            float acc = load_f(dtype, in[0], k);
+            for (int r = 1; r < P; r++) {
+                acc = acc + load_f(dtype, in[r], k);
+                if (dtype == ORC_BF16)
+                    acc = orc_bf16_to_f32(orc_f32_to_bf16(acc));   /* the += lands in bf16 */
+            }
+            store_f(dtype, out, i, acc);
         } else {
             float acc = load_f(dtype, in[0], k);
             for (int r = 1; r < P; r++)

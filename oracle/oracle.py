@@ -28,6 +28,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                        0 on it (the pages' [1,...,0,...,1] at g=1); no rank
                        released before all arrived.                     pinned
   barrier_step_model   the pages' edge-case table reproduced.          pinned
+  sum_stepwise         hand example (1 + 2^-8 + 2^-8 stays 1.0); equals a
+                       sequential torch bf16 `acc = acc + x`; P=2 and fp32
+                       equal SUM.                                       pinned
 """
 from __future__ import annotations
 
@@ -40,7 +43,7 @@ import numpy as np
 from . import build_oracle
 
 DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
-OPS = {"sum": 0, "avg": 1, "max": 2, "min": 3}
+OPS = {"sum": 0, "avg": 1, "max": 2, "min": 3, "sum_stepwise": 4}
 NP_DTYPE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}
 STATUS = {0: "ok", 1: "invalid", 2: "unsupported"}
 

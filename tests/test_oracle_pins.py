@@ -184,6 +184,34 @@ def test_bf16_accumulates_in_fp32_and_rounds_once_hand_example():
     assert int(out[0]) == 0x3F81
 
 
+def test_sum_stepwise_rounds_every_add_hand_example():
+    # the page's `result += tensor` in bf16: 1 + 2^-8 is a tie and rounds to 1.0
+    # (even), twice, so the result stays 0x3F80 where SUM gives 0x3F81
+    ins = [oracle.f32_to_bf16(f32([v])) for v in (1.0, 2.0 ** -8, 2.0 ** -8)]
+    assert int(oracle.reduce("bf16", "sum_stepwise", ins)[0]) == 0x3F80
+    assert int(oracle.reduce("bf16", "sum", ins)[0]) == 0x3F81
+
+
+@pytest.mark.parametrize("P", [2, 3, 5, 8, 16])
+def test_sum_stepwise_equals_sequential_torch_bf16_adds(P):
+    xs = [oracle.f32_to_bf16(rng.uniform(-1, 1, 2049).astype(np.float32)) for _ in range(P)]
+    t = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in xs]
+    acc = t[0].clone()
+    for r in range(1, P):
+        acc = acc + t[r]              # torch bf16 add: exact fp32 sum, one RNE to bf16
+    ref = acc.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.reduce("bf16", "sum_stepwise", xs), ref)
+
+
+def test_sum_stepwise_is_sum_for_two_ranks_fp32_and_int32():
+    xs = [oracle.f32_to_bf16(rng.uniform(-1, 1, 999).astype(np.float32)) for _ in range(2)]
+    assert np.array_equal(oracle.reduce("bf16", "sum_stepwise", xs), oracle.reduce("bf16", "sum", xs))
+    fs = [rng.uniform(-1, 1, 999).astype(np.float32) for _ in range(5)]
+    assert np.array_equal(oracle.reduce("f32", "sum_stepwise", fs), oracle.reduce("f32", "sum", fs))
+    ii = [rng.integers(-2 ** 31, 2 ** 31, 99, dtype=np.int64).astype(np.int32) for _ in range(5)]
+    assert np.array_equal(oracle.reduce("i32", "sum_stepwise", ii), oracle.reduce("i32", "sum", ii))
+
+
 def test_two_rank_fp32_sum_equals_torch_add():
     a = rng.standard_normal(4099).astype(np.float32) * 1e3
     b = rng.standard_normal(4099).astype(np.float32)
