@@ -83,8 +83,12 @@ typedef enum {
 
 typedef enum { DT_F32 = 0, DT_BF16 = 1, DT_I32 = 2 } dt_dtype;
 
-/* ReduceOpType of the ThreadGroup interface: kSum, kAvg, kMax, kMin. */
-typedef enum { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2, DT_MIN = 3 } dt_redop;
+/* ReduceOpType of the ThreadGroup interface: kSum, kAvg, kMax, kMin.
+ * DT_SUM_STEPWISE is the literal `result += DestGet(rank)` of the same-device
+ * AllReduce ("集合通信组件" §2.3): ranks added in ascending order with every
+ * add rounded to the element type, so bf16 rounds after each rank instead of
+ * once at the end; for fp32 and int32 it equals DT_SUM. */
+typedef enum { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2, DT_MIN = 3, DT_SUM_STEPWISE = 4 } dt_redop;
 
 #define DT_MAX_RANKS 16
 #define DT_ALL_RANKS (-1)

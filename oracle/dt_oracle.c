@@ -315,6 +315,82 @@ int orc_all_to_all(int P, const void *const *in, void *const *out, size_t chunk_
     return ORC_OK;
 }
 
+/* R -> S ([DT] §2.1 ReplicateToShard, §2.5 placement matrix R -> S): every
+ * rank holds the whole tensor (rows x row_bytes); the rows split evenly into P
+ * blocks and rank r keeps block shard_idx[r] (its own rank when shard_idx is
+ * NULL). */
+int orc_replicate_to_shard(int P, const void *const *in, void *const *out, const int *shard_idx,
+                           size_t rows, size_t row_bytes)
+{
+    if (P < 1 || P > ORC_MAX_RANKS || rows % (size_t)P)
+        return ORC_INVALID;
+    size_t block = rows / (size_t)P * row_bytes;
+    for (int r = 0; r < P; r++) {
+        int sidx = shard_idx ? shard_idx[r] : r;
+        if (sidx < 0 || sidx >= P)
+            return ORC_INVALID;
+        const unsigned char *src = (const unsigned char *)in[r] + (size_t)sidx * block;
+        unsigned char *dst = out[r];
+        for (size_t b = 0; b < block; b++)
+            dst[b] = src[b];
+    }
+    return ORC_OK;
+}
+
+/* S -> R as a vector ([DT] §2.1 AllGatherIntoVec): every rank keeps every
+ * rank's shard as a tensor of its own: out[q * P + r] is rank r's shard as
+ * received by rank q (rows[r] rows of row_bytes). */
+int orc_all_gather_into_vec(int P, const void *const *in, void *const *out, const size_t *rows,
+                            size_t row_bytes)
+{
+    if (P < 1 || P > ORC_MAX_RANKS || !rows)
+        return ORC_INVALID;
+    for (int q = 0; q < P; q++)
+        for (int r = 0; r < P; r++) {
+            const unsigned char *src = in[r];
+            unsigned char *dst = out[q * P + r];
+            for (size_t b = 0; b < rows[r] * row_bytes; b++)
+                dst[b] = src[b];
+        }
+    return ORC_OK;
+}
+
+/* S(src_dim) -> S(dest_dim) ([DT] §2.1 AllToAll(input, srcDim, destDim),
+ * §2.5 S -> S) for 2-D tensors of R x C elements of es bytes, row-major.
+ * Rank i splits its tensor X_i along dest_dim into P equal parts; part j goes
+ * to rank j, which concatenates the parts it receives along src_dim in
+ * ascending source rank.  A part is h x w (h = R/P or R, w = C or C/P); rank
+ * j's output is (P h) x w when src_dim is 0, h x (P w) when it is 1. */
+int orc_all_to_all_2d(int P, const void *const *in, void *const *out, size_t R, size_t C,
+                      size_t es, int src_dim, int dest_dim)
+{
+    if (P < 1 || P > ORC_MAX_RANKS || (src_dim != 0 && src_dim != 1) ||
+        (dest_dim != 0 && dest_dim != 1))
+        return ORC_INVALID;
+    if ((dest_dim == 0 && R % (size_t)P) || (dest_dim == 1 && C % (size_t)P))
+        return ORC_INVALID;
+    size_t h = dest_dim == 0 ? R / P : R;
+    size_t w = dest_dim == 1 ? C / P : C;
+    size_t out_rows = src_dim == 0 ? (size_t)P * h : h;
+    size_t out_cols = src_dim == 1 ? (size_t)P * w : w;
+    for (int j = 0; j < P; j++)
+        for (size_t a = 0; a < out_rows; a++)
+            for (size_t b = 0; b < out_cols; b++) {
+                /* which source rank, and where inside its part */
+                size_t i = src_dim == 0 ? a / h : b / w;
+                size_t pa = src_dim == 0 ? a % h : a;
+                size_t pb = src_dim == 1 ? b % w : b;
+                /* the part is block j of X_i along dest_dim */
+                size_t xa = pa + (dest_dim == 0 ? (size_t)j * h : 0);
+                size_t xb = pb + (dest_dim == 1 ? (size_t)j * w : 0);
+                const unsigned char *src = (const unsigned char *)in[i] + (xa * C + xb) * es;
+                unsigned char *dst = (unsigned char *)out[j] + (a * out_cols + b) * es;
+                for (size_t k = 0; k < es; k++)
+                    dst[k] = src[k];
+            }
+    return ORC_OK;
+}
+
 /* Bucket plan ([PB] §六.5: gradients are gathered into buckets of at most
  * bucket_cap bytes before one all-reduce per bucket).  Greedy in the given
  * order; writes bucket_of[t] and returns the number of buckets in *n_buckets. */

@@ -28,6 +28,13 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                        0 on it (the pages' [1,...,0,...,1] at g=1); no rank
                        released before all arrived.                     pinned
   barrier_step_model   the pages' edge-case table reproduced.          pinned
+  replicate_to_shard   equals torch.chunk(x, P)[r]; gathering the shards
+                       gives the tensor back.                           pinned
+  all_gather_into_vec  each entry equals the source shard; concatenated
+                       it is all_gather's output.                       pinned
+  all_to_all_2d        equals torch.cat of torch.chunk for all four
+                       (src, dest) pairs; (0,0) equals all_to_all; the
+                       (s,d) then (d,s) round trip is the identity.     pinned
   sum_stepwise         hand example (1 + 2^-8 + 2^-8 stays 1.0); equals a
                        sequential torch bf16 `acc = acc + x`; P=2 and fp32
                        equal SUM.                                       pinned
@@ -68,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.orc_all_gather.argtypes = [i, vpp, vpp, szp, sz]
         L.orc_all_to_all.argtypes = [i, vpp, vpp, sz]
         L.orc_all_gather_one.argtypes = [i, vpp, vp, szp, sz]
+        L.orc_replicate_to_shard.argtypes = [i, vpp, vpp, ctypes.POINTER(ctypes.c_int), sz, sz]
+        L.orc_all_gather_into_vec.argtypes = [i, vpp, vpp, szp, sz]
+        L.orc_all_to_all_2d.argtypes = [i, vpp, vpp, sz, sz, sz, i, i]
         L.orc_bucket_plan.argtypes = [szp, sz, sz, sz, szp, szp]
         L.orc_bucket_allreduce.argtypes = [i, i, i, vpp, szp, sz]
         L.orc_barrier_sim.argtypes = [i, i, ctypes.POINTER(ctypes.c_int32),
@@ -78,7 +88,8 @@ def lib() -> ctypes.CDLL:
         L.orc_bf16_to_f32.restype = ctypes.c_float
         L.orc_f32_to_bf16_array.argtypes = [vp, vp, sz]
         for name in ("orc_reduce", "orc_allreduce", "orc_reduce_scatter", "orc_all_gather",
-                     "orc_all_gather_one",
+                     "orc_all_gather_one", "orc_replicate_to_shard", "orc_all_gather_into_vec",
+                     "orc_all_to_all_2d",
                      "orc_all_to_all", "orc_bucket_plan", "orc_bucket_allreduce",
                      "orc_barrier_sim"):
             getattr(L, name).restype = ctypes.c_int
@@ -177,6 +188,46 @@ def all_gather_one(inputs: Sequence[np.ndarray], rows: Sequence[int], row_bytes:
     _check(lib().orc_all_gather_one(P, _ptrs(ins), out.ctypes.data, rows_c, row_bytes),
            "all_gather_one")
     return out
+
+
+def replicate_to_shard(inputs: Sequence[np.ndarray], rows: int, row_bytes: int,
+                       shard_idx: Sequence[int] | None = None) -> list:
+    """Rank r keeps row block shard_idx[r] (default r) of its whole tensor."""
+    ins = [np.ascontiguousarray(a).reshape(-1).view(np.uint8) for a in inputs]
+    P = len(ins)
+    if rows % P:
+        raise OracleError("replicate_to_shard: rows not a multiple of P")
+    outs = [np.empty(rows // P * row_bytes, dtype=np.uint8) for _ in range(P)]
+    sidx = None if shard_idx is None else (ctypes.c_int * P)(*shard_idx)
+    _check(lib().orc_replicate_to_shard(P, _ptrs(ins), _ptrs(outs), sidx, rows, row_bytes),
+           "replicate_to_shard")
+    return outs
+
+
+def all_gather_into_vec(inputs: Sequence[np.ndarray], rows: Sequence[int], row_bytes: int) -> list:
+    """out[q * P + r]: rank r's shard as held by rank q (uint8)."""
+    ins = [np.ascontiguousarray(a).reshape(-1).view(np.uint8) for a in inputs]
+    P = len(ins)
+    outs = [np.empty(rows[r] * row_bytes, dtype=np.uint8) for _ in range(P) for r in range(P)]
+    rows_c = (ctypes.c_size_t * P)(*rows)
+    _check(lib().orc_all_gather_into_vec(P, _ptrs(ins), _ptrs(outs), rows_c, row_bytes),
+           "all_gather_into_vec")
+    return outs
+
+
+def all_to_all_2d(inputs: Sequence[np.ndarray], src_dim: int, dest_dim: int) -> list:
+    """S(src_dim) -> S(dest_dim) on 2-D arrays; returns 2-D arrays of the input dtype."""
+    ins = [np.ascontiguousarray(a) for a in inputs]
+    P = len(ins)
+    R, C = ins[0].shape
+    es = ins[0].dtype.itemsize
+    h = R // P if dest_dim == 0 else R
+    w = C // P if dest_dim == 1 else C
+    shape = (P * h, w) if src_dim == 0 else (h, P * w)
+    outs = [np.empty(shape, dtype=ins[0].dtype) for _ in range(P)]
+    _check(lib().orc_all_to_all_2d(P, _ptrs(ins), _ptrs(outs), R, C, es, src_dim, dest_dim),
+           "all_to_all_2d")
+    return outs
 
 
 def all_to_all(inputs: Sequence[np.ndarray]) -> list:

@@ -79,7 +79,7 @@ using dt::DevError;
 
 size_t elem_bytes(int dtype) { return dtype == DT_BF16 ? 2 : 4; }
 bool valid_dtype(int dtype) { return dtype == DT_F32 || dtype == DT_BF16 || dtype == DT_I32; }
-bool valid_op(int op) { return op >= DT_SUM && op <= DT_MIN; }
+bool valid_op(int op) { return op >= DT_SUM && op <= DT_SUM_STEPWISE; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Switch to the group's device for the duration of a call.

@@ -8,7 +8,8 @@
 // narrowing at the store; AVG divides the fp32 sum by P (the hyper-parallel
 // page divides each reduced gradient by the replicate world size); int32
 // sums wrap.  MAX / MIN select an input element: a NaN wins, equal values
-// keep the lower rank's element.
+// keep the lower rank's element.  SUM_STEPWISE is the page's literal `+=` in
+// the element type: bf16 rounds after every rank.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -51,10 +52,16 @@ __device__ __forceinline__ bool take_f(float x, float best)
     return (x != x) || (OP == DT_MAX ? x > best : x < best);
 }
 
+// fp32 -> bf16 (round to nearest even) -> fp32: where a stepwise sum lands.
+__device__ __forceinline__ float round_bf16(float f)
+{
+    return __uint_as_float((uint32_t)f32_to_bf16(f) << 16);
+}
+
 template <int OP>
 __device__ __forceinline__ int32_t pick_i(int32_t acc, int32_t x)
 {
-    if (OP == DT_SUM) return (int32_t)((uint32_t)acc + (uint32_t)x);
+    if (OP == DT_SUM || OP == DT_SUM_STEPWISE) return (int32_t)((uint32_t)acc + (uint32_t)x);
     if (OP == DT_MAX) return x > acc ? x : acc;
     return x < acc ? x : acc;
 }
@@ -86,7 +93,8 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
             for (int r = 1; r < PMAX; ++r) {
                 if (r < P) {
                     float x1 = __uint_as_float(w[r][k]);
-                    if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x1);
+                    if constexpr (OP == DT_SUM || OP == DT_AVG || OP == DT_SUM_STEPWISE)
+                        acc = __fadd_rn(acc, x1);
                     else acc = take_f<OP>(x1, acc) ? x1 : acc;
                 }
             }
@@ -96,13 +104,17 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
     } else {  // bf16: two elements per 32-bit word, low half first
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            if constexpr (OP == DT_SUM || OP == DT_AVG) {
+            if constexpr (OP == DT_SUM || OP == DT_AVG || OP == DT_SUM_STEPWISE) {
                 float lo = bf16_lo(w[0][k]), hi = bf16_hi(w[0][k]);
 #pragma unroll
                 for (int r = 1; r < PMAX; ++r) {
                     if (r < P) {
                         lo = __fadd_rn(lo, bf16_lo(w[r][k]));
                         hi = __fadd_rn(hi, bf16_hi(w[r][k]));
+                        if constexpr (OP == DT_SUM_STEPWISE) {
+                            lo = round_bf16(lo);
+                            hi = round_bf16(hi);
+                        }
                     }
                 }
                 if constexpr (OP == DT_AVG) {
@@ -147,7 +159,7 @@ __device__ __forceinline__ void reduce_elem(const void *const *base, uint64_t in
         float acc = static_cast<const float *>(base[0])[j];
         for (int r = 1; r < P; ++r) {
             const float x = static_cast<const float *>(base[r])[j];
-            if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x);
+            if constexpr (OP == DT_SUM || OP == DT_AVG || OP == DT_SUM_STEPWISE) acc = __fadd_rn(acc, x);
             else acc = take_f<OP>(x, acc) ? x : acc;
         }
         if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
@@ -157,10 +169,11 @@ __device__ __forceinline__ void reduce_elem(const void *const *base, uint64_t in
         for (int r = 1; r < P; ++r) {
             const float x = bf16_to_f32(static_cast<const uint16_t *>(base[r])[j]);
             if constexpr (OP == DT_SUM || OP == DT_AVG) acc = __fadd_rn(acc, x);
+            else if constexpr (OP == DT_SUM_STEPWISE) acc = round_bf16(__fadd_rn(acc, x));
             else acc = take_f<OP>(x, acc) ? x : acc;
         }
         uint16_t b;
-        if constexpr (OP == DT_SUM || OP == DT_AVG) {
+        if constexpr (OP == DT_SUM || OP == DT_AVG || OP == DT_SUM_STEPWISE) {
             if constexpr (OP == DT_AVG) acc = avg_of(acc, P, scale, pow2);
             b = f32_to_bf16(acc);
         } else {

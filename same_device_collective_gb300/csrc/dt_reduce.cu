@@ -117,6 +117,11 @@ KernelInfo pick_op(int op, int P, bool vec)
         if constexpr (DT != DT_I32)
             k = vec ? pick_vec<DT, DT_AVG>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_AVG>, 1};
         break;
+    case DT_SUM_STEPWISE:   // only bf16 rounds between adds; the launcher maps the rest to SUM
+        if constexpr (DT == DT_BF16)
+            k = vec ? pick_vec<DT, DT_SUM_STEPWISE>(P)
+                    : KernelInfo{reduce_scalar_kernel<DT, DT_SUM_STEPWISE>, 1};
+        break;
     default: break;
     }
     return k;
@@ -128,6 +133,7 @@ cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bo
                           int device, cudaStream_t s)
 {
     KernelInfo k;
+    if (op == DT_SUM_STEPWISE && dtype != DT_BF16) op = DT_SUM;   // identical results
     if (dtype == DT_F32) k = pick_op<DT_F32>(op, p.P, vec);
     else if (dtype == DT_BF16) k = pick_op<DT_BF16>(op, p.P, vec);
     else if (dtype == DT_I32) k = pick_op<DT_I32>(op, p.P, vec);

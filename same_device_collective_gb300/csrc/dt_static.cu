@@ -65,7 +65,7 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     if (dtype != DT_BF16 && dtype != DT_F32)
         return dtype == DT_I32 ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
     if (op != DT_SUM && op != DT_AVG)
-        return (op == DT_MAX || op == DT_MIN) ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
+        return (op >= DT_SUM && op <= DT_SUM_STEPWISE) ? DT_ERR_UNSUPPORTED : DT_ERR_INVALID;
     if (n_tensors && (!grads || !counts)) return DT_ERR_INVALID;
     const int P = world_size;
     const size_t es = dtype == DT_BF16 ? 2 : 4;

@@ -28,14 +28,15 @@ _lib = ctypes.CDLL(LIB_PATH)
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_CUDA, DT_ERR_TIMEOUT, DT_ERR_OOM, \
     DT_ERR_POISONED, DT_ERR_TOO_LARGE = range(8)
 DT_F32, DT_BF16, DT_I32 = 0, 1, 2
-DT_SUM, DT_AVG, DT_MAX, DT_MIN = 0, 1, 2, 3
+DT_SUM, DT_AVG, DT_MAX, DT_MIN, DT_SUM_STEPWISE = 0, 1, 2, 3, 4
 DT_MAX_RANKS = 16
 DT_ALL_RANKS = -1
 DT_SHARED_OUTPUT = 0x1
 DT_DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
 DTYPES = {"f32": DT_F32, "bf16": DT_BF16, "i32": DT_I32}
-OPS = {"sum": DT_SUM, "avg": DT_AVG, "max": DT_MAX, "min": DT_MIN}
+OPS = {"sum": DT_SUM, "avg": DT_AVG, "max": DT_MAX, "min": DT_MIN,
+       "sum_stepwise": DT_SUM_STEPWISE}
 
 _vp = ctypes.c_void_p
 _vpp = ctypes.POINTER(ctypes.c_void_p)

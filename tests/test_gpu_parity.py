@@ -114,6 +114,30 @@ def test_allreduce_nan_and_signed_zero(dt):
     assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "i32"])
+@pytest.mark.parametrize("P", [2, 3, 8, 16])
+def test_sum_stepwise_matches_oracle(dt, dtype, P):
+    # the page's literal `result += tensor`: bf16 rounds after every rank
+    for seed, n in enumerate([7, 4096 * P + 5]):
+        xs = rand_inputs(P, n, dtype, 500 + seed)
+        outs = [torch.empty_like(x) for x in xs]
+        m = n // P
+        rs = [torch.empty(m, dtype=TORCH_DTYPE[dtype], device="cuda") for _ in range(P)]
+        with group(P) as g:
+            dt.dt_allreduce(g, dt.DT_ALL_RANKS, xs, outs, n, dtype, "sum_stepwise")
+            if m:
+                dt.dt_reduce_scatter(g, dt.DT_ALL_RANKS, xs, rs, m, dtype, "sum_stepwise")
+            torch.cuda.synchronize()
+        hx = [host(x) for x in xs]
+        want = oracle.allreduce(dtype, "sum_stepwise", hx)
+        for q in range(P):
+            assert_same(host(outs[q]), want[q], f"AR n={n} rank {q}")
+        if m:
+            want = oracle.reduce_scatter(dtype, "sum_stepwise", [h[:m * P] for h in hx])
+            for r in range(P):
+                assert_same(host(rs[r]), want[r], f"RS m={m} rank {r}")
+
+
 # ----------------------------------------------------------- ReduceScatter
 @pytest.mark.parametrize("dtype,op", DTYPE_OPS)
 @pytest.mark.parametrize("P", [2, 3, 4, 8, 16])

@@ -425,6 +425,69 @@ def test_all_to_all_twice_is_identity(P):
         assert np.array_equal(x, y)
 
 
+# --------------------------------------- ReplicateToShard, IntoVec, 2-D A2A
+@pytest.mark.parametrize("P", [1, 2, 4, 5])
+def test_replicate_to_shard_equals_torch_chunk_and_gathers_back(P):
+    rows, cols = 6 * P, 7
+    x = rng.integers(0, 255, (rows, cols), dtype=np.uint8)
+    outs = oracle.replicate_to_shard([x] * P, rows, cols)
+    for r in range(P):
+        assert np.array_equal(outs[r], torch.chunk(torch.from_numpy(x), P, 0)[r].numpy().reshape(-1))
+    back = oracle.all_gather(outs)
+    assert np.array_equal(back[0], x.reshape(-1))
+    # an explicit shard index picks another block
+    outs = oracle.replicate_to_shard([x] * P, rows, cols, shard_idx=[P - 1 - r for r in range(P)])
+    assert np.array_equal(outs[0], torch.chunk(torch.from_numpy(x), P, 0)[P - 1].numpy().reshape(-1))
+    if P > 1:
+        with pytest.raises(oracle.OracleError):
+            oracle.replicate_to_shard([x] * P, rows + 1, cols)
+
+
+@pytest.mark.parametrize("P", [1, 3, 4])
+def test_all_gather_into_vec_entries_and_concatenation(P):
+    rows = [2 + r for r in range(P)]
+    xs = [rng.integers(0, 255, rows[r] * 8, dtype=np.uint8) for r in range(P)]
+    vec = oracle.all_gather_into_vec(xs, rows, 8)
+    for q in range(P):
+        for r in range(P):
+            assert np.array_equal(vec[q * P + r], xs[r])
+        assert np.array_equal(np.concatenate(vec[q * P:(q + 1) * P]),
+                              oracle.all_gather(xs, rows, 8)[q])
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+@pytest.mark.parametrize("src_dim,dest_dim", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_all_to_all_2d_equals_torch_chunk_cat(P, src_dim, dest_dim):
+    R, C = 4 * P, 6 * P
+    xs = [rng.integers(-1000, 1000, (R, C)).astype(np.int32) for _ in range(P)]
+    outs = oracle.all_to_all_2d(xs, src_dim, dest_dim)
+    ts = [torch.from_numpy(x) for x in xs]
+    for j in range(P):
+        ref = torch.cat([torch.chunk(t, P, dest_dim)[j] for t in ts], src_dim)
+        assert np.array_equal(outs[j], ref.numpy())
+    back = oracle.all_to_all_2d(outs, dest_dim, src_dim)
+    for x, b in zip(xs, back):
+        assert np.array_equal(x, b)
+
+
+def test_all_to_all_2d_dim0_equals_flat_all_to_all():
+    P = 4
+    xs = [rng.integers(0, 255, (8, 12), dtype=np.uint8) for _ in range(P)]
+    a = oracle.all_to_all_2d(xs, 0, 0)
+    b = oracle.all_to_all(xs)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.reshape(-1), y)
+
+
+def test_planted_wrong_split_dim_is_caught():
+    P = 2
+    xs = [rng.integers(0, 255, (4, 6), dtype=np.uint8) for _ in range(P)]
+    mutant = oracle.all_to_all_2d(xs, 0, 0)            # split along the wrong dim
+    ts = [torch.from_numpy(x) for x in xs]
+    ref = torch.cat([torch.chunk(t, P, 1)[0] for t in ts], 0).numpy()
+    assert mutant[0].shape != ref.shape or not np.array_equal(mutant[0], ref)
+
+
 # ----------------------------------------------------------- buckets
 def test_bucket_plan_hand_cases():
     assert oracle.bucket_plan([10, 10, 10], 2, 40) == ([0, 0, 1], 2)
