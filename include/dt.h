@@ -176,6 +176,38 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
 dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *const *out,
                         size_t chunk_bytes, void *stream);
 
+/* ReplicateToShard (R -> S): "集合通信组件" §2.1 ReplicateToShard(input,
+ * shardIdx) and the R -> S entry of the §2.5 placement matrix.  Every rank
+ * holds the whole tensor (rows rows of row_bytes bytes, rows a multiple of
+ * P); rank r keeps row block shard_idx[r] (NULL: block r) of the P equal
+ * blocks: out[r] = in[r][shard_idx[r] * rows/P, (shard_idx[r] + 1) * rows/P).
+ * Byte copies.  Rank-local: shard_idx points at the calling rank's own index
+ * (NULL: its rank).  The sub-split coordinate of the page (nested meshes) is
+ * not modelled. */
+dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, void *const *out,
+                                const int *shard_idx, size_t rows, size_t row_bytes, void *stream);
+
+/* AllGatherIntoVec (S -> R, kept apart): "集合通信组件" §2.1
+ * AllGatherIntoVec: every rank receives every rank's shard as a tensor of
+ * its own.  out has P * P entries; out[q * P + r] (rows[r] rows, or
+ * rows_equal when rows is NULL, of row_bytes bytes) receives rank r's shard
+ * on rank q.  Rank-local: out has the calling rank's P entries, rows must be
+ * NULL and rows_equal is the rank's own row count. */
+dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, void *const *out,
+                                 const size_t *rows, size_t rows_equal, size_t row_bytes,
+                                 void *stream);
+
+/* AllToAll(srcDim, destDim) (S(src_dim) -> S(dest_dim)): "集合通信组件"
+ * §2.1 AllToAll(input, srcDim, destDim) on 2-D tensors of R x C elements of
+ * elem_bytes bytes (row-major).  Rank i splits its tensor along dest_dim into
+ * P equal parts (h x w: R/P x C or R x C/P); part j goes to rank j, which
+ * concatenates the parts it receives along src_dim in ascending source rank:
+ * out[j] is (P h) x w for src_dim 0 and h x (P w) for src_dim 1.
+ * (0, 0) is dt_all_to_all with chunk_bytes = R/P * C * elem_bytes. */
+dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *const *out,
+                           size_t R, size_t C, size_t elem_bytes, int src_dim, int dest_dim,
+                           void *stream);
+
 /* Fused gradient-bucket all-reduce: "异步融合 AllReduce 流水线优化"
  * (AllReduceParamGroup.issue_async_allreduce / wait_and_apply_grads: SUM
  * all-reduce of the fused gradient buffer, each gradient view then divided by

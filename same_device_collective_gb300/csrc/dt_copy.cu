@@ -21,8 +21,8 @@
 namespace dt {
 namespace {
 
-template <int NSEG>
-__device__ __forceinline__ int find_seg(const CopyParams<NSEG> &p, uint64_t tile)
+template <typename Params>
+__device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
 {
     int lo = 0, hi = p.nseg - 1;      // last segment with tile_begin <= tile
     while (lo < hi) {
@@ -47,9 +47,9 @@ constexpr int kBulkTile = 32768;
 constexpr int kBulkThreads = 32;
 constexpr size_t kBulkSmem = 128 + (size_t)kBulkStages * kBulkTile;
 
-template <int NSEG>
+template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kBulkThreads)
-copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG> p)
+copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_begin();
@@ -106,9 +106,9 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG> p)
 }
 
 // Any alignment: byte by byte, same tiling.
-template <int NSEG>
+template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kThreads)
-copy_byte_kernel(const __grid_constant__ CopyParams<NSEG> p)
+copy_byte_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
     pdl_begin();
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
@@ -123,13 +123,13 @@ copy_byte_kernel(const __grid_constant__ CopyParams<NSEG> p)
     }
 }
 
-template <int NSEG>
-cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec,
+template <int NSEG, int NOUT>
+cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
                      const ErrorSink &sink, int device, cudaStream_t s)
 {
-    CopyParams<NSEG> p;
+    CopyParams<NSEG, NOUT> p;
     memset(&p, 0, sizeof p);
-    for (int r = 0; r < DT_MAX_RANKS; ++r) p.out[r] = out[r];
+    for (int r = 0; r < nout && r < NOUT; ++r) p.out[r] = out[r];
     p.sink = sink;
     p.tile_bytes = vec ? (uint64_t)kBulkTile : 4096;
     uint64_t tiles = 0;
@@ -146,7 +146,7 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec,
     p.total_tiles = tiles;
 
     if (vec) {
-        void (*fn)(CopyParams<NSEG>) = copy_bulk_kernel<NSEG>;
+        void (*fn)(CopyParams<NSEG, NOUT>) = copy_bulk_kernel<NSEG, NOUT>;
         static bool attr_set = false;   // per instantiation; the attribute is per function
         if (!attr_set) {
             cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
@@ -162,7 +162,7 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec,
         const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
         return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), kBulkSmem, s, false, p);
     }
-    void (*fn)(CopyParams<NSEG>) = copy_byte_kernel<NSEG>;
+    void (*fn)(CopyParams<NSEG, NOUT>) = copy_byte_kernel<NSEG, NOUT>;
     int resident = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
     if (e != cudaSuccess) return e;
@@ -172,12 +172,77 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, bool vec,
 
 }  // namespace
 
-cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec,
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
                         const ErrorSink &sink, int device, cudaStream_t s)
 {
-    if (nseg <= DT_MAX_RANKS) return launch_n<DT_MAX_RANKS>(segs, nseg, out, vec, sink, device, s);
-    if (nseg <= kMaxSeg) return launch_n<kMaxSeg>(segs, nseg, out, vec, sink, device, s);
+    if (nout > DT_MAX_RANKS) {
+        if (nseg > DT_MAX_RANKS || nout > kMaxSeg) return cudaErrorInvalidValue;
+        return launch_n<DT_MAX_RANKS, kMaxSeg>(segs, nseg, out, nout, vec, sink, device, s);
+    }
+    if (nseg <= DT_MAX_RANKS) return launch_n<DT_MAX_RANKS, DT_MAX_RANKS>(segs, nseg, out, nout, vec, sink, device, s);
+    if (nseg <= kMaxSeg) return launch_n<kMaxSeg, DT_MAX_RANKS>(segs, nseg, out, nout, vec, sink, device, s);
     return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// 2-D copy: a tile is rows_per_tile whole rows of one segment; warp w of the
+// block copies rows w, w + 8, ... of the tile, its lanes striding over the
+// row in 16-byte vectors (kVec) or bytes.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant__ Copy2dParams p)
+{
+    pdl_begin();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+        const Copy2dSeg &sg = p.seg[find_seg(p, tile)];
+        const uint64_t r0 = (tile - sg.tile_begin) * sg.rows_per_tile;
+        const uint64_t r1 = r0 + sg.rows_per_tile < sg.rows ? r0 + sg.rows_per_tile : sg.rows;
+        unsigned char *dbase = static_cast<unsigned char *>(p.out[sg.dst]) + sg.dst_off;
+        for (uint64_t row = r0 + warp; row < r1; row += kThreads / 32) {
+            const unsigned char *src = sg.src + row * sg.src_pitch;
+            unsigned char *dst = dbase + row * sg.dst_pitch;
+            if (kVec) {
+                const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                for (uint64_t v = lane; v < sg.row_bytes / 16; v += 32) __stcs(d4 + v, __ldcs(s4 + v));
+            } else {
+                for (uint64_t b = lane; b < sg.row_bytes; b += 32) dst[b] = src[b];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, bool vec, int device,
+                          cudaStream_t s)
+{
+    if (nseg > DT_MAX_RANKS * DT_MAX_RANKS) return cudaErrorInvalidValue;
+    Copy2dParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r < DT_MAX_RANKS; ++r) p.out[r] = out[r];
+    uint64_t tiles = 0;
+    int used = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (segs[i].rows == 0 || segs[i].row_bytes == 0) continue;
+        p.seg[used] = segs[i];
+        uint64_t rpt = 16384 / segs[i].row_bytes;   // about 16 KiB per tile
+        if (rpt < 1) rpt = 1;
+        p.seg[used].rows_per_tile = rpt;
+        p.seg[used].tile_begin = tiles;
+        tiles += (segs[i].rows + rpt - 1) / rpt;
+        ++used;
+    }
+    if (used == 0) return cudaSuccess;
+    p.nseg = used;
+    p.total_tiles = tiles;
+    void (*fn)(Copy2dParams) = vec ? copy2d_kernel<true> : copy2d_kernel<false>;
+    int resident = 0;
+    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
+    if (e != cudaSuccess) return e;
+    const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
+    return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
 }
 
 }  // namespace dt

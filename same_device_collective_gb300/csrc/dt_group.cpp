@@ -215,14 +215,20 @@ size_t plan_buckets(const size_t *counts, size_t T, size_t es, size_t cap, size_
     return T ? b + 1 : 0;
 }
 
-enum CallKind { CK_ALLREDUCE = 1, CK_REDUCE_SCATTER, CK_ALL_GATHER, CK_ALL_TO_ALL, CK_BARRIER };
+enum CallKind {
+    CK_ALLREDUCE = 1, CK_REDUCE_SCATTER, CK_ALL_GATHER, CK_ALL_TO_ALL, CK_BARRIER,
+    CK_REPLICATE_TO_SHARD, CK_ALL_GATHER_INTO_VEC, CK_ALL_TO_ALL_2D
+};
 
 bool same_call(const dt_group::RankCall &a, const dt_group::RankCall &b)
 {
     // every rank of a round must make the same call; an uneven AllGather's
     // row counts are each rank's own
-    return a.kind == b.kind && a.dtype == b.dtype && a.op == b.op && a.flags == b.flags &&
-           a.row_bytes == b.row_bytes && (a.kind == CK_ALL_GATHER || a.count == b.count);
+    const bool own_rows = a.kind == CK_ALL_GATHER || a.kind == CK_ALL_GATHER_INTO_VEC;
+    const bool own_op = a.kind == CK_REPLICATE_TO_SHARD;   // op holds the rank's shard index
+    return a.kind == b.kind && a.dtype == b.dtype && (own_op || a.op == b.op) &&
+           a.flags == b.flags && a.dim2 == b.dim2 && a.row_bytes == b.row_bytes &&
+           (own_rows || a.count == b.count);
 }
 
 // The last rank of a round launches the group-wide call on its own stream,
@@ -256,6 +262,20 @@ dt_status launch_round(dt_group *g, int last)
         return dt_all_to_all(g, DT_ALL_RANKS, ins, outs, c0.count, s);
     case CK_BARRIER:
         return dt_barrier(g, DT_ALL_RANKS, s);
+    case CK_REPLICATE_TO_SHARD: {
+        int shard[DT_MAX_RANKS];
+        for (int r = 0; r < P; ++r) shard[r] = g->rv_call[r].op;
+        return dt_replicate_to_shard(g, DT_ALL_RANKS, ins, outs, shard, c0.count, c0.row_bytes, s);
+    }
+    case CK_ALL_GATHER_INTO_VEC: {
+        void *vec[DT_MAX_RANKS * DT_MAX_RANKS];
+        for (int q = 0; q < P; ++q)
+            for (int r = 0; r < P; ++r) vec[q * P + r] = g->rv_call[q].outv[r];
+        return dt_all_gather_into_vec(g, DT_ALL_RANKS, ins, vec, rows, 0, c0.row_bytes, s);
+    }
+    case CK_ALL_TO_ALL_2D:
+        return dt_all_to_all_2d(g, DT_ALL_RANKS, ins, outs, c0.count, c0.row_bytes,
+                                (size_t)c0.dtype, c0.op, c0.dim2, s);
     }
     return DT_ERR_INVALID;
 }
@@ -334,6 +354,8 @@ dt_group::RankCall make_call(int kind, const void *const *in, void *const *out, 
     c.kind = kind;
     c.in = in ? in[0] : nullptr;
     c.out = out ? out[0] : nullptr;
+    c.outv = out;
+    c.dim2 = 0;
     c.count = count;
     c.row_bytes = row_bytes;
     c.dtype = dtype;
@@ -675,7 +697,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
     }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs, P, outs, vec, error_sink(g), g->device,
+    return cuda_status(dt::launch_copy(segs, P, outs, nout, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -730,7 +752,7 @@ dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *con
     for (int q = 0; q < P; ++q) outs[q] = out[q];
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, vec, error_sink(g), g->device,
+    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, P, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -876,6 +898,199 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     g->plan_used[k] = true;
     if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(e2);
+}
+
+dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, void *const *out,
+                                const int *shard_idx, size_t rows, size_t row_bytes, void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out) return DT_ERR_INVALID;
+        const int own = shard_idx ? shard_idx[0] : rank;
+        return rank_local(g, rank, make_call(CK_REPLICATE_TO_SHARD, in, out, rows, row_bytes, 0, own,
+                                             0, stream));
+    }
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (!in || !out) return DT_ERR_INVALID;
+    const int P = g->P;
+    if (rows % (size_t)P || (row_bytes && rows > SIZE_MAX / 4 / row_bytes)) return DT_ERR_INVALID;
+    const size_t block = rows / P * row_bytes, whole = rows * row_bytes;
+    int sidx[DT_MAX_RANKS];
+    for (int r = 0; r < P; ++r) {
+        sidx[r] = shard_idx ? shard_idx[r] : r;
+        if (sidx[r] < 0 || sidx[r] >= P) return DT_ERR_INVALID;
+        if (block && (!in[r] || !out[r])) return DT_ERR_INVALID;
+    }
+    if (block == 0) return DT_OK;
+    for (int q = 0; q < P; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + block, q, 1};
+        for (int r = 0; r < P; ++r) {
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + whole, r, 0};
+            if (overlaps(o, i)) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < P; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + block, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+    dt::CopySeg segs[DT_MAX_RANKS];
+    void *outs[DT_MAX_RANKS] = {};
+    bool vec = block % 16 == 0;
+    for (int r = 0; r < P; ++r) {
+        segs[r].src = static_cast<const unsigned char *>(in[r]) + (size_t)sidx[r] * block;
+        segs[r].bytes = block;
+        segs[r].dst_off = 0;
+        segs[r].tile_begin = 0;
+        segs[r].dst_first = r;
+        segs[r].dst_count = 1;
+        outs[r] = out[r];
+        vec = vec && aligned16(in[r]) && aligned16(out[r]);
+    }
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_copy(segs, P, outs, P, vec, error_sink(g), g->device,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, void *const *out,
+                                 const size_t *rows, size_t rows_equal, size_t row_bytes,
+                                 void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out || rows) return DT_ERR_INVALID;
+        return rank_local(g, rank, make_call(CK_ALL_GATHER_INTO_VEC, in, out, rows_equal, row_bytes, 0,
+                                             0, 0, stream));
+    }
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (!in || !out) return DT_ERR_INVALID;
+    const int P = g->P;
+    size_t nb[DT_MAX_RANKS];
+    for (int r = 0; r < P; ++r) {
+        const size_t n = rows ? rows[r] : rows_equal;
+        if (row_bytes && n > SIZE_MAX / 4 / row_bytes) return DT_ERR_INVALID;
+        nb[r] = n * row_bytes;
+        if (nb[r] && !in[r]) return DT_ERR_INVALID;
+        for (int q = 0; q < P; ++q)
+            if (nb[r] && !out[q * P + r]) return DT_ERR_INVALID;
+    }
+    // no destination may overlap a source or another destination
+    std::vector<Range> ranges;
+    for (int r = 0; r < P; ++r) {
+        if (!nb[r]) continue;
+        ranges.push_back({(uintptr_t)in[r], (uintptr_t)in[r] + nb[r], r, 0});
+        for (int q = 0; q < P; ++q)
+            ranges.push_back({(uintptr_t)out[q * P + r], (uintptr_t)out[q * P + r] + nb[r], q, 1});
+    }
+    if (ranges.empty()) return DT_OK;
+    // sweep in start order: an output may not start before the end of any
+    // earlier range, an input not before the end of any earlier output
+    // (inputs may overlap each other: they are only read)
+    std::sort(ranges.begin(), ranges.end(), [](const Range &a, const Range &b) { return a.lo < b.lo; });
+    uintptr_t end_any = 0, end_out = 0;
+    for (const Range &r : ranges) {
+        if (r.kind == 1 ? r.lo < end_any : r.lo < end_out) return DT_ERR_INVALID;
+        end_any = std::max(end_any, r.hi);
+        if (r.kind == 1) end_out = std::max(end_out, r.hi);
+    }
+
+    // segment r: rank r's shard to out[q * P + r] for every q; the table is
+    // stored by source (outs[r * P + q]) so a segment's destinations are adjacent
+    dt::CopySeg segs[DT_MAX_RANKS];
+    std::vector<void *> outs((size_t)P * P);
+    bool vec = true;
+    for (int r = 0; r < P; ++r) {
+        segs[r].src = static_cast<const unsigned char *>(in[r]);
+        segs[r].bytes = nb[r];
+        segs[r].dst_off = 0;
+        segs[r].tile_begin = 0;
+        segs[r].dst_first = r * P;
+        segs[r].dst_count = P;
+        if (nb[r]) vec = vec && aligned16(in[r]) && nb[r] % 16 == 0;
+        for (int q = 0; q < P; ++q) {
+            outs[(size_t)r * P + q] = out[q * P + r];
+            if (nb[r]) vec = vec && aligned16(out[q * P + r]);
+        }
+    }
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_copy(segs, P, outs.data(), P * P, vec, error_sink(g), g->device,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *const *out,
+                           size_t R, size_t C, size_t elem_bytes, int src_dim, int dest_dim,
+                           void *stream)
+{
+    if (!g) return DT_ERR_INVALID;
+    if (rank != DT_ALL_RANKS) {
+        if (!in || !out) return DT_ERR_INVALID;
+        dt_group::RankCall c = make_call(CK_ALL_TO_ALL_2D, in, out, R, C, (int)elem_bytes, src_dim, 0,
+                                         stream);
+        c.dim2 = dest_dim;
+        return rank_local(g, rank, c);
+    }
+    if ((src_dim != 0 && src_dim != 1) || (dest_dim != 0 && dest_dim != 1) || elem_bytes == 0 ||
+        elem_bytes > 16)
+        return DT_ERR_INVALID;
+    if (src_dim == 0 && dest_dim == 0) {
+        if (R % (size_t)g->P) return DT_ERR_INVALID;
+        return dt_all_to_all(g, DT_ALL_RANKS, in, out, R / g->P * C * elem_bytes, stream);
+    }
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (!in || !out) return DT_ERR_INVALID;
+    const int P = g->P;
+    if ((dest_dim == 0 && R % (size_t)P) || (dest_dim == 1 && C % (size_t)P)) return DT_ERR_INVALID;
+    if (C && R > SIZE_MAX / 4 / C / elem_bytes) return DT_ERR_INVALID;
+    const size_t es = elem_bytes, bytes = R * C * es;
+    for (int r = 0; r < P; ++r)
+        if (bytes && (!in[r] || !out[r])) return DT_ERR_INVALID;
+    if (bytes == 0) return DT_OK;
+    for (int q = 0; q < P; ++q) {
+        const Range o{(uintptr_t)out[q], (uintptr_t)out[q] + bytes, q, 1};
+        for (int r = 0; r < P; ++r) {
+            const Range i{(uintptr_t)in[r], (uintptr_t)in[r] + bytes, r, 0};
+            if (overlaps(o, i)) return DT_ERR_INVALID;
+        }
+        for (int k = q + 1; k < P; ++k) {
+            const Range o2{(uintptr_t)out[k], (uintptr_t)out[k] + bytes, k, 1};
+            if (overlaps(o, o2)) return DT_ERR_INVALID;
+        }
+    }
+    // the part of rank i bound for rank j: h x w elements (h = R/P or R,
+    // w = C or C/P) at (j h, 0) or (0, j w) of X_i; it lands at row i h
+    // (src_dim 0, output width w) or column i w (src_dim 1, output width P w)
+    const size_t h = dest_dim == 0 ? R / P : R, w = dest_dim == 1 ? C / P : C;
+    const size_t out_w = src_dim == 1 ? (size_t)P * w : w;
+    std::vector<dt::Copy2dSeg> segs((size_t)P * P);
+    bool vec = (w * es) % 16 == 0 && (C * es) % 16 == 0 && (out_w * es) % 16 == 0;
+    for (int i = 0; i < P; ++i) {
+        vec = vec && aligned16(in[i]) && aligned16(out[i]);
+        for (int j = 0; j < P; ++j) {
+            dt::Copy2dSeg &sg = segs[(size_t)i * P + j];
+            memset(&sg, 0, sizeof sg);
+            const size_t src_off = dest_dim == 0 ? (size_t)j * h * C : (size_t)j * w;
+            sg.src = static_cast<const unsigned char *>(in[i]) + src_off * es;
+            sg.src_pitch = C * es;
+            sg.dst = j;
+            sg.dst_off = (src_dim == 0 ? (size_t)i * h * out_w : (size_t)i * w) * es;
+            sg.dst_pitch = out_w * es;
+            sg.rows = h;
+            sg.row_bytes = w * es;
+        }
+    }
+    void *outs[DT_MAX_RANKS] = {};
+    for (int q = 0; q < P; ++q) outs[q] = out[q];
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(dt::launch_copy2d(segs.data(), P * P, outs, vec, g->device,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 dt_status dt_barrier(dt_group_t g, int rank, void *stream)

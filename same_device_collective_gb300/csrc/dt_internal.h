@@ -65,15 +65,39 @@ struct CopySeg {
     int32_t dst_count;
 };
 
-template <int NSEG>
+template <int NSEG, int NOUT = DT_MAX_RANKS>
 struct CopyParams {
-    void *out[DT_MAX_RANKS];
+    void *out[NOUT];
     ErrorSink sink;
     uint64_t tile_bytes;
     uint64_t total_tiles;
     int32_t nseg;
     int32_t pad;
     CopySeg seg[NSEG];
+};
+
+// ---- 2-D strided copies (AllToAll along other dims) -----------------------
+// Segment s copies `rows` rows of row_bytes from src (row pitch src_pitch) to
+// out[dst] + dst_off (row pitch dst_pitch).  Tiles are runs of whole rows.
+struct Copy2dSeg {
+    const unsigned char *src;
+    uint64_t src_pitch;
+    uint64_t dst_off;
+    uint64_t dst_pitch;
+    uint64_t rows;
+    uint64_t row_bytes;
+    uint64_t rows_per_tile;
+    uint64_t tile_begin;
+    int32_t dst;
+    int32_t pad;
+};
+
+struct Copy2dParams {
+    void *out[DT_MAX_RANKS];
+    uint64_t total_tiles;
+    int32_t nseg;
+    int32_t pad;
+    Copy2dSeg seg[DT_MAX_RANKS * DT_MAX_RANKS];
 };
 
 // ---- fused bucket all-reduce ----------------------------------------------
@@ -166,8 +190,12 @@ cudaError_t resident_blocks(const void *fn, int threads, int device, int *out,
 
 cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bool vec,
                           int device, cudaStream_t s);
-cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, bool vec,
+// nout destinations in `out` (up to DT_MAX_RANKS, or DT_MAX_RANKS^2 for the
+// vector form of AllGather)
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
                         const ErrorSink &sink, int device, cudaStream_t s);
+cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, bool vec, int device,
+                          cudaStream_t s);
 cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s);
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s);
 cudaError_t launch_ring(const RingParams &p, cudaStream_t s);
@@ -217,9 +245,11 @@ struct dt_group {
         int kind;                 // which collective (dt_group.cpp: CallKind)
         const void *in;
         void *out;
-        size_t count;             // elements / recv_count / this rank's rows / chunk bytes
-        size_t row_bytes;
-        int dtype, op;
+        void *const *outv;        // AllGatherIntoVec: this rank's P outputs
+        size_t count;             // elements / recv_count / this rank's rows / chunk bytes / R
+        size_t row_bytes;         // row bytes / C (2-D AllToAll)
+        int dtype, op;            // dtype or element bytes; op, shard index or src_dim
+        int dim2;                 // dest_dim (2-D AllToAll)
         unsigned flags;
         cudaStream_t stream;
     };

@@ -65,6 +65,9 @@ _SIGS = {
     "dt_bucket_plan": ([_szp, _sz, _sz, _sz, _szp, _szp], _i),
     "dt_bucket_allreduce_static": ([_i, _vpp, _szp, _sz, _i, _i, _sz, _vp], _i),
     "dt_barrier": ([_vp, _i, _vp], _i),
+    "dt_replicate_to_shard": ([_vp, _i, _vpp, _vpp, ctypes.POINTER(_i), _sz, _sz, _vp], _i),
+    "dt_all_gather_into_vec": ([_vp, _i, _vpp, _vpp, _szp, _sz, _sz, _vp], _i),
+    "dt_all_to_all_2d": ([_vp, _i, _vpp, _vpp, _sz, _sz, _sz, _i, _i, _vp], _i),
     "dt_debug_read_window": ([_vp, ctypes.POINTER(ctypes.c_int32), _vp], _i),
     "dt_debug_ring_after_barrier": ([_vp, _vpp, _vpp, _vpp, _sz, _vp], _i),
     "dt_debug_barrier_expect": ([_vp, _i, _u32, _vp], _i),
@@ -202,6 +205,28 @@ def dt_all_to_all(g: int, rank: int, ins: Sequence, outs: Sequence, chunk_bytes:
                   stream=None) -> None:
     _check(_lib.dt_all_to_all(g, rank, _ptr_array(ins), _ptr_array(outs), chunk_bytes,
                               _stream(stream)), "dt_all_to_all")
+
+
+def dt_replicate_to_shard(g: int, rank: int, ins: Sequence, outs: Sequence, shard_idx, rows: int,
+                          row_bytes: int, stream=None) -> None:
+    sidx = None if shard_idx is None else (ctypes.c_int * max(len(shard_idx), 1))(*shard_idx)
+    _check(_lib.dt_replicate_to_shard(g, rank, _ptr_array(ins), _ptr_array(outs), sidx, rows,
+                                      row_bytes, _stream(stream)), "dt_replicate_to_shard")
+
+
+def dt_all_gather_into_vec(g: int, rank: int, ins: Sequence, outs: Sequence, rows: Sequence | None,
+                           rows_equal: int, row_bytes: int, stream=None) -> None:
+    """outs[q * P + r] receives rank r's shard on rank q (rank-local: P entries)."""
+    rows_arr = None if rows is None else (ctypes.c_size_t * max(len(rows), 1))(*rows)
+    _check(_lib.dt_all_gather_into_vec(g, rank, _ptr_array(ins), _ptr_array(outs), rows_arr,
+                                       rows_equal, row_bytes, _stream(stream)),
+           "dt_all_gather_into_vec")
+
+
+def dt_all_to_all_2d(g: int, rank: int, ins: Sequence, outs: Sequence, R: int, C: int,
+                     elem_bytes: int, src_dim: int, dest_dim: int, stream=None) -> None:
+    _check(_lib.dt_all_to_all_2d(g, rank, _ptr_array(ins), _ptr_array(outs), R, C, elem_bytes,
+                                 src_dim, dest_dim, _stream(stream)), "dt_all_to_all_2d")
 
 
 def dt_bucket_allreduce(g: int, grads: Sequence[Sequence], counts: Sequence[int], dtype, op,
