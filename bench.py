@@ -244,7 +244,7 @@ def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
 
 
 ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "uneven_all_gather",
-             "barrier", "rank_local"]
+             "barrier", "rank_local", "placements"]
 
 
 def measure_rows(dt, dev, peak, only=None):
@@ -436,6 +436,37 @@ def measure_rows(dt, dev, peak, only=None):
             "frac_of_measured_hbm": round(gbs / peak, 4), "threads": P, "status_ok": ok,
             "timing": "wall clock over K steps, both ends synchronised"}
         del w, xs, rs, ag
+
+    # Remaining placement conversions at the configured shapes: R -> S of a
+    # replicated bf16 [8192, 4096] tensor (P=4), AllGatherIntoVec of its
+    # shards, S(0) -> S(1) AllToAll of P=8 bf16 [65536, 4096] token matrices,
+    # and the page-literal stepwise bf16 sum as a ReduceScatter (P=4).
+    if want("placements"):
+        P, R, C = P_RANKS, ROWS, COLS
+        gen = torch.Generator(device=dev).manual_seed(1)
+        full = [torch.randn(R, C, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
+        shards = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        g = dt.dt_group_create(P, dev.index)
+        ms = time_events(lambda: dt.dt_replicate_to_shard(g, ALL, full, shards, None, R, C * 2), 20)
+        rec("replicate_to_shard_bf16_P4_8192x4096", 2 * R * C * 2, ms)
+        vec = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P * P)]
+        ms = time_events(lambda: dt.dt_all_gather_into_vec(g, ALL, shards, vec, None, R // P, C * 2), 20)
+        rec("all_gather_into_vec_bf16_P4_2048x4096", (P + P * P) * (R // P) * C * 2, ms)
+        del vec
+        rsb = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ms = time_events(lambda: dt.dt_reduce_scatter(g, ALL, full, rsb, R // P * C, "bf16",
+                                                      "sum_stepwise"), 20)
+        rec("reduce_scatter_sum_stepwise_bf16_P4_8192x4096", (P + 1) * R * C * 2, ms)
+        dt.dt_group_destroy(g)
+        del full, shards, rsb
+        w = workloads.all_to_all_tokens(device=str(dev))
+        R8, C8 = w.inputs[0].shape
+        outs = [torch.empty(8 * R8, C8 // 8, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        g = dt.dt_group_create(8, dev.index)
+        ms = time_events(lambda: dt.dt_all_to_all_2d(g, ALL, w.inputs, outs, R8, C8, 2, 0, 1), 10)
+        rec("all_to_all_S0_to_S1_bf16_P8_65536x4096", 2 * 8 * R8 * C8 * 2, ms)
+        dt.dt_group_destroy(g)
+        del w, outs
 
     torch.cuda.empty_cache()
     return rows

@@ -69,6 +69,7 @@ extern "C" {
 #endif
 
 typedef struct dt_group *dt_group_t;
+typedef struct dt_work *dt_work_t;
 
 typedef enum {
     DT_OK = 0,
@@ -78,7 +79,8 @@ typedef enum {
     DT_ERR_TIMEOUT = 4,      /* a device-side wait ran out of time (see dt_group_check) */
     DT_ERR_OOM = 5,          /* the group could not allocate its own state */
     DT_ERR_POISONED = 6,     /* an earlier timeout left the group unusable until reset */
-    DT_ERR_TOO_LARGE = 7     /* request exceeds the fixed scratch of dt_bucket_allreduce_static */
+    DT_ERR_TOO_LARGE = 7,    /* request exceeds the fixed scratch of dt_bucket_allreduce_static */
+    DT_NOT_READY = 8         /* dt_work_query: the work has not finished yet (not an error) */
 } dt_status;
 
 typedef enum { DT_F32 = 0, DT_BF16 = 1, DT_I32 = 2 } dt_dtype;
@@ -266,6 +268,32 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
 dt_status dt_bucket_allreduce_static(int world_size, void *const *grads, const size_t *counts,
                                      size_t n_tensors, int dtype, int op,
                                      size_t bucket_cap_bytes, void *stream);
+
+/* ----------------------------------------------------------- async work */
+
+/* Asynchronous collectives, after the async mode of "通信与互联（05）" §四.3
+ * (async_op=True): the collective runs on the backend's own stream, which
+ * first waits for the caller's stream (syncStream), and the caller gets a
+ * Work whose end event it waits on later; §五.5's rule holds: buffers of an
+ * unfinished work are neither read nor written on any stream.
+ *   dt_async_begin  makes the group's communication stream wait for the work
+ *                   already on `stream` and returns that communication stream
+ *                   in *comm_stream: pass it to the dt_* calls of the scope
+ *                   (any collective, any number); one scope per group at a
+ *                   time, opened and closed by one thread
+ *   dt_async_end    closes the scope and returns a work handle whose end
+ *                   event covers everything enqueued in the scope
+ *   dt_work_wait    makes `stream` wait for the work (no host blocking)
+ *   dt_work_query   DT_OK when the work has finished, DT_NOT_READY if not
+ *   dt_work_free    returns the handle to its group (after waiting or
+ *                   querying; freeing does not cancel the work)
+ * Groups on different communication streams (for example the shard and
+ * replicate groups of an HSDP mesh) run their works concurrently. */
+dt_status dt_async_begin(dt_group_t g, void *stream, void **comm_stream);
+dt_status dt_async_end(dt_group_t g, dt_work_t *work);
+dt_status dt_work_wait(dt_work_t work, void *stream);
+dt_status dt_work_query(dt_work_t work);
+dt_status dt_work_free(dt_work_t work);
 
 /* ------------------------------------------------------------- test hooks */
 

@@ -179,6 +179,12 @@ void destroy_all(dt_group *g)
         release_plan_slot(g, k);
         if (g->plan_done[k]) cudaEventDestroy(g->plan_done[k]);
     }
+    for (dt_work *w : g->work_all) {
+        if (w->end) cudaEventDestroy(w->end);
+        delete w;
+    }
+    if (g->scope_start) cudaEventDestroy(g->scope_start);
+    if (g->comm) cudaStreamDestroy(g->comm);
     for (int r = 0; r < DT_MAX_RANKS; ++r)
         if (g->rv_ready[r]) cudaEventDestroy(g->rv_ready[r]);
     for (int k = 0; k < 2; ++k)
@@ -380,6 +386,7 @@ const char *dt_status_string(dt_status st)
     case DT_ERR_OOM: return "out of memory";
     case DT_ERR_POISONED: return "group poisoned by an earlier device error; reset it";
     case DT_ERR_TOO_LARGE: return "request exceeds the fixed scratch of the allocation-free entry point";
+    case DT_NOT_READY: return "work not finished yet";
     }
     return "unknown status";
 }
@@ -423,6 +430,8 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
         e = cudaEventCreateWithFlags(&g->rv_ready[r], cudaEventDisableTiming);
     for (int k = 0; k < 2 && e == cudaSuccess; ++k)
         e = cudaEventCreateWithFlags(&g->rv_done[k], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g->comm, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->scope_start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         destroy_all(g);
@@ -1105,6 +1114,86 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream)
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
     return issue_barrier(g, static_cast<cudaStream_t>(stream));
+}
+
+dt_status dt_async_begin(dt_group_t g, void *stream, void **comm_stream)
+{
+    if (!g || !comm_stream) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    dt_status st = take_device_error(g);
+    if (st != DT_OK) return st;
+    if (g->scope_open) return DT_ERR_INVALID;
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    // syncStream: the communication stream waits for the caller's stream
+    cudaError_t e = cudaEventRecord(g->scope_start, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(g->comm, g->scope_start, 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    g->scope_open = true;
+    *comm_stream = g->comm;
+    return DT_OK;
+}
+
+dt_status dt_async_end(dt_group_t g, dt_work_t *work)
+{
+    if (!g || !work) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g->mu);
+    if (!g->scope_open) return DT_ERR_INVALID;
+    DeviceScope scope(g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    dt_work *w = nullptr;
+    if (!g->work_free.empty()) {
+        w = g->work_free.back();
+        g->work_free.pop_back();
+    } else {
+        w = new (std::nothrow) dt_work;
+        if (!w) return DT_ERR_OOM;
+        w->g = g;
+        cudaError_t e = cudaEventCreateWithFlags(&w->end, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            delete w;
+            return cuda_status(e);
+        }
+        g->work_all.push_back(w);
+    }
+    cudaError_t e = cudaEventRecord(w->end, g->comm);
+    g->scope_open = false;
+    if (e != cudaSuccess) {
+        g->work_free.push_back(w);
+        return cuda_status(e);
+    }
+    *work = w;
+    return DT_OK;
+}
+
+dt_status dt_work_wait(dt_work_t w, void *stream)
+{
+    if (!w || !w->g) return DT_ERR_INVALID;
+    DeviceScope scope(w->g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    return cuda_status(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), w->end, 0));
+}
+
+dt_status dt_work_query(dt_work_t w)
+{
+    if (!w || !w->g) return DT_ERR_INVALID;
+    DeviceScope scope(w->g->device);
+    if (!scope.ok) return DT_ERR_CUDA;
+    const cudaError_t e = cudaEventQuery(w->end);
+    if (e == cudaSuccess) return DT_OK;
+    if (e == cudaErrorNotReady) {
+        (void)cudaGetLastError();   // a not-ready query is not an error
+        return DT_NOT_READY;
+    }
+    return DT_ERR_CUDA;
+}
+
+dt_status dt_work_free(dt_work_t w)
+{
+    if (!w || !w->g) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(w->g->mu);
+    w->g->work_free.push_back(w);
+    return DT_OK;
 }
 
 dt_status dt_debug_read_window(dt_group_t g, int32_t *host_out, void *stream)

@@ -202,6 +202,14 @@ cudaError_t launch_ring(const RingParams &p, cudaStream_t s);
 
 }  // namespace dt
 
+struct dt_group;
+
+// An asynchronous work: the end event of one async scope.
+struct dt_work {
+    dt_group *g = nullptr;
+    cudaEvent_t end = nullptr;
+};
+
 // The group object behind dt_group_t.
 struct dt_group {
     int P = 0;
@@ -263,6 +271,14 @@ struct dt_group {
     dt_status rv_status[2] = {DT_OK, DT_OK};
     cudaEvent_t rv_ready[DT_MAX_RANKS] = {};
     cudaEvent_t rv_done[2] = {nullptr, nullptr};
+
+    // async scopes: the communication stream, the scope's start event and a
+    // pool of work handles (each owns an end event)
+    cudaStream_t comm = nullptr;
+    cudaEvent_t scope_start = nullptr;
+    bool scope_open = false;
+    std::vector<dt_work *> work_free;
+    std::vector<dt_work *> work_all;
 
     std::mutex mu;
 };

@@ -26,7 +26,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 DT_OK, DT_ERR_INVALID, DT_ERR_UNSUPPORTED, DT_ERR_CUDA, DT_ERR_TIMEOUT, DT_ERR_OOM, \
-    DT_ERR_POISONED, DT_ERR_TOO_LARGE = range(8)
+    DT_ERR_POISONED, DT_ERR_TOO_LARGE, DT_NOT_READY = range(9)
 DT_F32, DT_BF16, DT_I32 = 0, 1, 2
 DT_SUM, DT_AVG, DT_MAX, DT_MIN, DT_SUM_STEPWISE = 0, 1, 2, 3, 4
 DT_MAX_RANKS = 16
@@ -68,6 +68,11 @@ _SIGS = {
     "dt_replicate_to_shard": ([_vp, _i, _vpp, _vpp, ctypes.POINTER(_i), _sz, _sz, _vp], _i),
     "dt_all_gather_into_vec": ([_vp, _i, _vpp, _vpp, _szp, _sz, _sz, _vp], _i),
     "dt_all_to_all_2d": ([_vp, _i, _vpp, _vpp, _sz, _sz, _sz, _i, _i, _vp], _i),
+    "dt_async_begin": ([_vp, _vp, ctypes.POINTER(_vp)], _i),
+    "dt_async_end": ([_vp, ctypes.POINTER(_vp)], _i),
+    "dt_work_wait": ([_vp, _vp], _i),
+    "dt_work_query": ([_vp], _i),
+    "dt_work_free": ([_vp], _i),
     "dt_debug_read_window": ([_vp, ctypes.POINTER(ctypes.c_int32), _vp], _i),
     "dt_debug_ring_after_barrier": ([_vp, _vpp, _vpp, _vpp, _sz, _vp], _i),
     "dt_debug_barrier_expect": ([_vp, _i, _u32, _vp], _i),
@@ -262,6 +267,35 @@ def dt_bucket_plan(counts: Sequence[int], elem_bytes: int, cap_bytes: int):
 
 def dt_barrier(g: int, rank: int = DT_ALL_RANKS, stream=None) -> None:
     _check(_lib.dt_barrier(g, rank, _stream(stream)), "dt_barrier")
+
+
+def dt_async_begin(g: int, stream=None) -> int:
+    """Open an async scope; returns the communication stream handle (int)."""
+    cs = ctypes.c_void_p()
+    _check(_lib.dt_async_begin(g, _stream(stream), ctypes.byref(cs)), "dt_async_begin")
+    return cs.value or 0
+
+
+def dt_async_end(g: int) -> int:
+    w = ctypes.c_void_p()
+    _check(_lib.dt_async_end(g, ctypes.byref(w)), "dt_async_end")
+    return w.value
+
+
+def dt_work_wait(work: int, stream=None) -> None:
+    _check(_lib.dt_work_wait(work, _stream(stream)), "dt_work_wait")
+
+
+def dt_work_query(work: int) -> int:
+    """DT_OK when finished, DT_NOT_READY otherwise (does not raise for those)."""
+    st = _lib.dt_work_query(work)
+    if st not in (DT_OK, DT_NOT_READY):
+        raise DtError(st, "dt_work_query")
+    return st
+
+
+def dt_work_free(work: int) -> None:
+    _check(_lib.dt_work_free(work), "dt_work_free")
 
 
 def dt_debug_read_window(g: int, stream=None):
