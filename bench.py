@@ -244,7 +244,7 @@ def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
 
 
 ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "uneven_all_gather",
-             "barrier", "rank_local", "placements"]
+             "barrier", "rank_local", "placements", "hsdp_pipeline"]
 
 
 def measure_rows(dt, dev, peak, only=None):
@@ -467,6 +467,111 @@ def measure_rows(dt, dev, peak, only=None):
         rec("all_to_all_S0_to_S1_bf16_P8_65536x4096", 2 * 8 * R8 * C8 * 2, ms)
         dt.dt_group_destroy(g)
         del w, outs
+
+    # Async works: the hyper-parallel post_backward schedule on a 2 x 2 mesh of
+    # logical ranks (two shard groups, two replicate groups), 8 modules of
+    # bf16 gradients (32 Mi elements per rank per module); each module's
+    # backward compute is stood in for by a bf16 GEMM on the compute stream.
+    # Sequential: compute, ReduceScatter, AllReduce per module on one stream.
+    # Pipelined: the same work with the collectives in async scopes on the
+    # groups' own streams (wait previous RS, issue RS, issue previous AR).
+    if want("hsdp_pipeline"):
+        M, n = 8, 32 << 20
+        gen = torch.Generator(device=dev).manual_seed(7)
+        grads = [[torch.randn(n, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
+                 for _ in range(M)]
+        rsb = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)] for _ in range(M)]
+        fin = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)] for _ in range(M)]
+        a = torch.randn(8192, 8192, generator=gen, device=dev).to(torch.bfloat16)
+        b = torch.randn(8192, 4096, generator=gen, device=dev).to(torch.bfloat16)
+        c = torch.empty(8192, 4096, dtype=torch.bfloat16, device=dev)
+        shard = [dt.dt_group_create(2, dev.index) for _ in range(2)]
+        repl = [dt.dt_group_create(2, dev.index) for _ in range(2)]
+        compute = torch.cuda.Stream(dev)
+        craw = compute.cuda_stream
+
+        def rs_of(m, stream):
+            for s_ in range(2):
+                x, y = 2 * s_, 2 * s_ + 1
+                dt.dt_reduce_scatter(shard[s_], ALL, [grads[m][x], grads[m][y]],
+                                     [rsb[m][x], rsb[m][y]], n // 2, "bf16", "avg", stream)
+
+        def ar_of(m, stream):
+            for k in range(2):
+                dt.dt_allreduce(repl[k], ALL, [rsb[m][k], rsb[m][k + 2]], [fin[m][k], fin[m][k + 2]],
+                                n // 2, "bf16", "avg", 0, stream)
+
+        def sequential():
+            with torch.cuda.stream(compute):
+                for m in range(M):
+                    torch.matmul(a, b, out=c)
+                    rs_of(m, craw)
+                    ar_of(m, craw)
+
+        def pipelined():
+            with torch.cuda.stream(compute):
+                prev, pend = [], []
+                for m in range(M):
+                    torch.matmul(a, b, out=c)                  # module m's backward
+                    for w_ in prev:
+                        dt.dt_work_wait(w_, compute)
+                        dt.dt_work_free(w_)
+                    cur = []
+                    for s_ in range(2):
+                        cs = dt.dt_async_begin(shard[s_], compute)
+                        x, y = 2 * s_, 2 * s_ + 1
+                        dt.dt_reduce_scatter(shard[s_], ALL, [grads[m][x], grads[m][y]],
+                                             [rsb[m][x], rsb[m][y]], n // 2, "bf16", "avg", cs)
+                        cur.append(dt.dt_async_end(shard[s_]))
+                    if m > 0:
+                        for k in range(2):
+                            cs = dt.dt_async_begin(repl[k], compute)
+                            dt.dt_allreduce(repl[k], ALL, [rsb[m - 1][k], rsb[m - 1][k + 2]],
+                                            [fin[m - 1][k], fin[m - 1][k + 2]], n // 2, "bf16", "avg", 0, cs)
+                            pend.append(dt.dt_async_end(repl[k]))
+                    prev = cur
+                for w_ in prev:
+                    dt.dt_work_wait(w_, compute)
+                    dt.dt_work_free(w_)
+                for k in range(2):
+                    cs = dt.dt_async_begin(repl[k], compute)
+                    dt.dt_allreduce(repl[k], ALL, [rsb[M - 1][k], rsb[M - 1][k + 2]],
+                                    [fin[M - 1][k], fin[M - 1][k + 2]], n // 2, "bf16", "avg", 0, cs)
+                    pend.append(dt.dt_async_end(repl[k]))
+                for w_ in pend:
+                    dt.dt_work_wait(w_, compute)
+                    dt.dt_work_free(w_)
+
+        def wall(fn, reps=5):
+            fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            return sorted(ts)[reps // 2]
+
+        def gemm_only():
+            with torch.cuda.stream(compute):
+                for _ in range(M):
+                    torch.matmul(a, b, out=c)
+
+        t_gemm = wall(gemm_only)
+        t_seq = wall(sequential)
+        t_pipe = wall(pipelined)
+        ok = all(dt.dt_group_check(x) == dt.DT_OK for x in shard + repl)
+        for x in shard + repl:
+            dt.dt_group_destroy(x)
+        comm_bytes = M * 2 * ((2 + 1) * n * 2 + 2 * 2 * (n // 2) * 2)
+        rows["hsdp_pipeline_2x2_bf16_M8"] = {
+            "us_sequential": round(t_seq * 1e6, 1), "us_pipelined": round(t_pipe * 1e6, 1),
+            "us_compute_only": round(t_gemm * 1e6, 1),
+            "speedup": round(t_seq / t_pipe, 3),
+            "comm_GB/s_sequential_excl_compute": round(comm_bytes / max(t_seq - t_gemm, 1e-9) / 1e9, 1),
+            "status_ok": ok, "timing": "wall clock, median of 5, synchronised"}
+        del grads, rsb, fin, a, b, c
 
     torch.cuda.empty_cache()
     return rows
