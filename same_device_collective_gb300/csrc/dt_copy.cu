@@ -42,15 +42,30 @@ __device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
 // Every mbarrier wait is bounded: a wait that runs out records DT_ERR_TIMEOUT
 // (rank -1, peer = tile), drains the loads still in flight with bounded waits
 // and returns.
-constexpr int kBulkStages = 6;
-constexpr int kBulkTile = 32768;
 constexpr int kBulkThreads = 32;
-constexpr size_t kBulkSmem = 128 + (size_t)kBulkStages * kBulkTile;
+
+// Tile size and pipeline depth per launch layout (measured on GB300): the
+// P^2 single-destination segments of an AllToAll stream best as 16 KiB tiles
+// 12 deep; gathers (few segments, several destinations each) as 32 KiB x 6.
+// Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
+// bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
+template <int NSEG>
+struct BulkShape {
+    static constexpr int kStages = NSEG > DT_MAX_RANKS ? 12 : 6;
+    static constexpr int kTile = NSEG > DT_MAX_RANKS ? 16384 : 32768;
+    static constexpr size_t kBarBytes = ((size_t)kStages * 8 + 127) / 128 * 128;
+    static constexpr size_t kSmem = kBarBytes + (size_t)kStages * kTile;
+    static_assert(kBarBytes >= (size_t)kStages * 8, "mbarrier area too small");
+    static_assert(kTile % 16 == 0 && kTile < (1 << 20), "bulk tile: 16-byte multiple, below the tx limit");
+    static_assert(kSmem <= 227 * 1024, "bulk copy shared memory above the per-block limit");
+};
 
 template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kBulkThreads)
 copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
+    constexpr int kBulkStages = BulkShape<NSEG>::kStages;
+    constexpr int kBulkTile = BulkShape<NSEG>::kTile;
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_begin();
     if (threadIdx.x != 0) return;
@@ -58,7 +73,7 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     if (first >= p.total_tiles) return;
     const uint64_t n = (p.total_tiles - first + step - 1) / step;   // tiles of this block
     const uint32_t bar0 = smem_addr(smem);
-    const uint32_t buf0 = smem_addr(smem + 128);
+    const uint32_t buf0 = smem_addr(smem + BulkShape<NSEG>::kBarBytes);
     for (int k = 0; k < kBulkStages; ++k) mbar_init(bar0 + 8 * k, 1);
     mbar_init_fence();
     const uint64_t pol = policy_evict_first();
@@ -131,7 +146,7 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
     memset(&p, 0, sizeof p);
     for (int r = 0; r < nout && r < NOUT; ++r) p.out[r] = out[r];
     p.sink = sink;
-    p.tile_bytes = vec ? (uint64_t)kBulkTile : 4096;
+    p.tile_bytes = vec ? (uint64_t)BulkShape<NSEG>::kTile : 4096;
     uint64_t tiles = 0;
     int used = 0;
     for (int i = 0; i < nseg; ++i) {
@@ -151,16 +166,17 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
         if (!attr_set) {
             cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)kBulkSmem);
+                                                 (int)BulkShape<NSEG>::kSmem);
             if (e != cudaSuccess) return e;
             attr_set = true;
         }
         int resident = 0;
         cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
-                                        &resident, kBulkSmem);
+                                        &resident, BulkShape<NSEG>::kSmem);
         if (e != cudaSuccess) return e;
         const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
-        return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), kBulkSmem, s, false, p);
+        return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), BulkShape<NSEG>::kSmem, s,
+                             false, p);
     }
     void (*fn)(CopyParams<NSEG, NOUT>) = copy_byte_kernel<NSEG, NOUT>;
     int resident = 0;
