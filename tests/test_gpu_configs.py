@@ -94,8 +94,10 @@ def test_config3_bucket_allreduce_avg_bf16_P8_full(dt, wl):
     counts = w.meta["counts"]
     ref = [[host(x).copy() for x in row] for row in w.inputs]
     _, nb = dt.dt_bucket_plan(counts, 2, wl.BUCKET_CAP_BYTES)
+    # the argument form the bench times: a prepared pointer table
+    table, cnt = dt.pointer_table(w.inputs), np.asarray(counts, dtype=np.uint64)
     with group(P) as g:
-        dt.dt_bucket_allreduce(g, w.inputs, counts, "bf16", "avg", wl.BUCKET_CAP_BYTES)
+        dt.dt_bucket_allreduce(g, table, cnt, "bf16", "avg", wl.BUCKET_CAP_BYTES)
         torch.cuda.synchronize()
         assert dt.dt_group_check(g) == dt.DT_OK
         assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, nb - 1))

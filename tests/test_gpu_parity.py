@@ -285,9 +285,11 @@ def test_bucket_plan_reuse_across_calls(dt):
                   .to(torch.bfloat16).cuda() for _ in range(P)] for c in counts]
         sets[name] = (counts, grads, [[host(x).copy() for x in row] for row in grads])
     with group(P) as g:
-        for name in ["A", "B", "A", "B", "A", "A"]:
+        for i, name in enumerate(["A", "B", "A", "B", "A", "A"]):
             counts, grads, ref = sets[name]
-            dt.dt_bucket_allreduce(g, grads, counts, "bf16", "sum", bucket_cap_bytes=64 << 10)
+            # alternate the nested-list and the prepared-table argument forms
+            arg = grads if i % 2 == 0 else dt.pointer_table(grads)
+            dt.dt_bucket_allreduce(g, arg, counts, "bf16", "sum", bucket_cap_bytes=64 << 10)
             oracle.bucket_allreduce("bf16", "sum", ref)
             torch.cuda.synchronize()
             for t in range(len(counts)):
