@@ -63,9 +63,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in files:
         with open(os.path.join(ROOT, "same_device_collective_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -73,13 +73,14 @@ def kernel_source_hash():
 
 def ncu_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, only while the
-    kernel sources are the ones the counters were taken on."""
+    sources the kernel is built from (the entry's src_files) are the ones the
+    counters were taken on."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[kernel_key]
-        if e.get("src_sha") == kernel_source_hash():
+        if e.get("src_sha") == kernel_source_hash(e.get("src_files", KERNEL_SOURCES)):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         pass
@@ -190,6 +191,67 @@ def time_oracle(rows_per_rank: int, min_seconds: float, max_reps: int):
         if el >= min_seconds or reps >= max_reps:
             break
     return (rs_b + ag_b) * reps / el / 1e9, el, reps
+
+
+def host_info():
+    """The host the CPU baseline ran on: logical CPUs and CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def time_oracle_configs(min_seconds: float = 1.0):
+    """The oracle, single-threaded, on a bounded sample of every other
+    configured workload but the RS+AG step (the headline's own sample); GB/s over
+    the same algorithmic bytes the GPU rows count."""
+    import oracle
+    from same_device_collective_gb300 import workloads
+
+    def rate(fn, nbytes):
+        fn()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds:
+                return round(nbytes * reps / el / 1e9, 4), reps
+
+    out = {}
+    xs = [x.numpy() for x in workloads.allreduce_small().inputs]
+    v, reps = rate(lambda: oracle.allreduce("f32", "sum", xs), 2 * 2 * xs[0].size * 4)
+    out["allreduce_sum_f32_P2_n2^20"] = {"GB/s": v, "reps": reps, "sample": "the full workload"}
+
+    w = workloads.bucket_grads(T=20)
+    grads = [[x.view(__import__("torch").int16).numpy().view(np.uint16) for x in row]
+             for row in w.inputs]
+    n = sum(w.meta["counts"])
+    v, reps = rate(lambda: oracle.bucket_allreduce("bf16", "avg", grads), 2 * 8 * n * 2)
+    out["bucket_allreduce_avg_bf16_P8"] = {
+        "GB/s": v, "reps": reps,
+        "sample": f"20 gradients ({n} bf16 elements per rank) drawn with the 200-tensor recipe"}
+
+    w = workloads.all_to_all_tokens(rows=8192)
+    ins = [x.view(__import__("torch").int16).numpy() for x in w.inputs]
+    v, reps = rate(lambda: oracle.all_to_all(ins), 2 * 8 * ins[0].size * 2)
+    out["all_to_all_bf16_P8"] = {"GB/s": v, "reps": reps,
+                                 "sample": "[8192, 4096] per rank (1/8 of the rows)"}
+
+    w = workloads.uneven_gather(max_rows=2048)
+    rws = w.meta["rows"]
+    ins = [x.numpy() for x in w.inputs]
+    v, reps = rate(lambda: oracle.all_gather(ins, rws, 4096 * 4), sum(rws) * 16384 * 9)
+    out["uneven_all_gather_i32_P8"] = {"GB/s": v, "reps": reps,
+                                       "sample": f"rows {rws} x 4096 (rows up to 2048)"}
+    return out
 
 
 def run_reference(args):
@@ -449,8 +511,22 @@ def measure_rows(dt, dev, peak, only=None):
         rows["rank_local_rs_ag_step_bf16_P4"] = {
             "GB/s": round(gbs, 1), "us_per_step": round(el / K * 1e6, 2), "steps": K,
             "frac_of_measured_hbm": round(gbs / peak, 4), "threads": P, "status_ok": ok,
-            "timing": "wall clock over K steps, both ends synchronised"}
+            "timing": "wall clock over K steps, both ends synchronised",
+            "caller": "Python threads (the interpreter lock serialises their argument handling)"}
         del w, xs, rs, ag
+        torch.cuda.synchronize()
+        # the same step from native threads: the library's own rank-local cost
+        tool = os.path.join(ROOT, "same_device_collective_gb300", "rank_local_step")
+        try:
+            res = subprocess.run([tool, str(P), str(R), str(C), "2000"], capture_output=True,
+                                 text=True, timeout=300)
+            native = json.loads(res.stdout.strip().splitlines()[-1])
+            if "GB/s" in native:
+                native["frac_of_measured_hbm"] = round(native["GB/s"] / peak, 4)
+            native["caller"] = "C++ std::thread per rank (rank_local_step)"
+        except (OSError, ValueError, IndexError, subprocess.TimeoutExpired) as ex:
+            native = {"error": f"{type(ex).__name__}: {ex}"}
+        rows["rank_local_rs_ag_step_bf16_P4_native_threads"] = native
 
     # Remaining placement conversions at the configured shapes: R -> S of a
     # replicated bf16 [8192, 4096] tensor (P=4), AllGatherIntoVec of its
@@ -654,6 +730,68 @@ def run_e2e(dt, g, xs, P, rows_, cols, m, steps, world, dev):
     return ms, value, h2d, d2h
 
 
+# Small invocations for ncu captures (the bench step itself serves its own
+# ReduceScatter and AllGather): the kernel regex, the warm-up launches of that
+# kernel to skip (-s) and what one case runs.  Sizes keep inputs larger than
+# L2 where the workload has them and the device footprint to a few GB.
+NCU_CASES = {
+    "allreduce_small": ("reduce_vec_kernel", 2, "AllReduce kSum f32, P=2, 2^20 per rank"),
+    "bucket": ("bucket_kernel", 14, "bucket AllReduce kAvg bf16, P=8, 200 tensors, 25 MiB buckets"),
+    "all_to_all": ("copy_bulk_kernel", 2, "AllToAll bf16, P=8, [8192, 4096] per rank"),
+    "uneven_all_gather": ("copy_bulk_kernel", 2,
+                          "uneven AllGather int32, P=8, rows U[1, 2048] x 4096, per-rank outputs"),
+    "barrier": ("barrier_kernel", 2, "signal-window barrier, P=16"),
+}
+
+
+def run_ncu_case(name):
+    """Two warm-up calls and three more of one collective, for an ncu capture
+    (-k <regex> -s <skip> from NCU_CASES).  Prints one JSON line."""
+    import torch
+    from same_device_collective_gb300 import dt, workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ALL = dt.DT_ALL_RANKS
+    if name == "allreduce_small":
+        xs = [x.to(dev) for x in workloads.allreduce_small().inputs]
+        outs = [torch.empty_like(x) for x in xs]
+        g = dt.dt_group_create(2, dev.index)
+        call = lambda: dt.dt_allreduce(g, ALL, xs, outs, xs[0].numel(), "f32", "sum")
+    elif name == "bucket":
+        w = workloads.bucket_grads(device=str(dev))
+        table = dt.pointer_table(w.inputs)
+        cnt = np.asarray(w.meta["counts"], dtype=np.uint64)
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_bucket_allreduce(g, table, cnt, "bf16", "avg",
+                                              workloads.BUCKET_CAP_BYTES)
+    elif name == "all_to_all":
+        w = workloads.all_to_all_tokens(rows=8192, device=str(dev))
+        outs = [torch.empty_like(x) for x in w.inputs]
+        nbytes = w.inputs[0].numel() * 2
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes // 8)
+    elif name == "uneven_all_gather":
+        w = workloads.uneven_gather(max_rows=2048, device=str(dev))
+        rws = w.meta["rows"]
+        outs = [torch.empty(sum(rws), 4096, dtype=torch.int32, device=dev) for _ in range(8)]
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_all_gather(g, ALL, w.inputs, outs, rws, 0, 4096 * 4)
+    elif name == "barrier":
+        g = dt.dt_group_create(16, dev.index)
+        call = lambda: dt.dt_barrier(g)
+    else:
+        raise ValueError(name)
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    st = dt.dt_group_check(g)
+    dt.dt_group_destroy(g)
+    regex, skip, what = NCU_CASES[name]
+    print(json.dumps({"ncu_case": name, "what": what, "calls": 5, "kernel_regex": regex,
+                      "skip_launches": skip, "status_ok": st == dt.DT_OK}))
+    return 0 if st == dt.DT_OK else 1
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -771,7 +909,8 @@ def run_ours(args):
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"RS(avg)+AG on {P} ranks x bf16 [1024, {COLS}] (1/8 of the workload's "
                          f"rows, drawn with the same recipe), {reps} reps in {el:.1f} s, "
-                         f"single-threaded C"}
+                         f"single-threaded C",
+               "host": host_info(), "per_config": time_oracle_configs()}
 
     if g is not None:
         dt.dt_group_destroy(g)
@@ -920,6 +1059,8 @@ def main(argv=None):
     ap.add_argument("--sweep-max-bytes", type=int, default=1 << 30)
     ap.add_argument("--row", choices=ROW_NAMES,
                     help="measure one collective at its own workload and print it")
+    ap.add_argument("--ncu-case", choices=sorted(NCU_CASES),
+                    help="run a few calls of one collective for an ncu capture (no timing)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -927,6 +1068,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.ncu_case:
+        return run_ncu_case(args.ncu_case)
     if args.row:
         import torch
         from same_device_collective_gb300 import dt

@@ -2,7 +2,8 @@
 
 Each source compiles to an object in parallel, then nvcc links the shared
 library next to this file.  The CUDA runtime is linked statically, so the
-library only needs the driver at run time.
+library only needs the driver at run time.  The rank_local_step program (the
+rank-local call pattern from native threads) is linked against it.
 """
 from __future__ import annotations
 
@@ -17,10 +18,12 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "dt")
 LIB = os.path.join(PKG, "libdt.so")
+# rank-local pattern from native threads, linked against libdt.so
+STEP_TOOL = os.path.join(PKG, "rank_local_step")
 
 SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu",
            "dt_static.cu"]
-HEADERS = ["dt_internal.h", "dt_math.cuh", "dt_device.cuh"]
+HEADERS = ["dt_internal.h", "dt_group.h", "dt_math.cuh", "dt_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the reductions use
@@ -77,6 +80,15 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
         os.replace(tmp, LIB)
+    tool_src = os.path.join(CSRC, "rank_local_step.cpp")
+    if force or _stale(STEP_TOOL, [tool_src, LIB, os.path.join(INCLUDE, "dt.h")]):
+        tmp = STEP_TOOL + f".tmp{os.getpid()}"
+        cmd = [nvcc(), "-O2", "-std=c++17", "-I", INCLUDE, "-x", "c++", tool_src, "-o", tmp,
+               "-L", PKG, "-ldt", "-Xlinker", "-rpath,$ORIGIN", "-lpthread"]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"rank_local_step build failed:\n{res.stdout}\n{res.stderr}")
+        os.replace(tmp, STEP_TOOL)
     return LIB
 
 

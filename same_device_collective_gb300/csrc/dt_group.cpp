@@ -20,7 +20,7 @@
 #include <utility>
 #include <vector>
 
-#include "dt_internal.h"
+#include "dt_group.h"
 
 namespace dt {
 

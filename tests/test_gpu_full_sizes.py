@@ -1,7 +1,8 @@
 """Parity at the workloads' full sizes, launched the way bench.py launches them.
 
-Where the oracle can take the whole problem on the host it does (configs 1-3,
-the uneven gather's single concatenation); where the problem is many GiB the
+Where the oracle can take the whole problem on the host it does (the P=2
+AllReduce, the RS+AG step, the bucket all-reduce, the uneven gather's single
+concatenation); where the problem is many GiB the
 check uses outputs the oracle computes one by one (sampled element positions
 of a reduction, sampled offsets of every all-to-all chunk) plus properties
 that hold at any size (all-to-all twice is the identity; every per-rank
@@ -51,8 +52,8 @@ def sample_reduce(dtype, op, ins, out, in_off, n, k=4096, seed=0):
     assert_same(got, want, f"sampled {dtype} {op}")
 
 
-# ------------------------------------------------------------- configs 1-4
-def test_config1_allreduce_sum_f32_P2(dt, wl):
+# ------------------------------------------------------- the full workloads
+def test_full_allreduce_sum_f32_P2_n2e20(dt, wl):
     w = wl.allreduce_small()
     xs = [x.cuda() for x in w.inputs]
     outs = [torch.empty_like(x) for x in xs]
@@ -64,7 +65,7 @@ def test_config1_allreduce_sum_f32_P2(dt, wl):
         assert_same(host(outs[q]), want[q], f"rank {q}")
 
 
-def test_config2_rs_avg_then_ag_bf16_P4_full(dt, wl):
+def test_full_rs_avg_then_ag_bf16_P4_8192x4096(dt, wl):
     P, R, C = 4, 8192, 4096
     w = wl.rs_ag(device="cuda")
     xs = w.inputs
@@ -88,7 +89,7 @@ def test_config2_rs_avg_then_ag_bf16_P4_full(dt, wl):
         assert_same(host(ag[q]), want_ag, f"all_gather rank {q}")
 
 
-def test_config3_bucket_allreduce_avg_bf16_P8_full(dt, wl):
+def test_full_bucket_allreduce_avg_bf16_P8_T200(dt, wl):
     P = 8
     w = wl.bucket_grads(device="cuda")
     counts = w.meta["counts"]
@@ -107,7 +108,7 @@ def test_config3_bucket_allreduce_avg_bf16_P8_full(dt, wl):
             assert_same(host(w.inputs[t][p]), ref[t][p], f"tensor {t} rank {p}")
 
 
-def test_config4a_all_to_all_bf16_P8_full(dt, wl):
+def test_full_all_to_all_bf16_P8_65536x4096(dt, wl):
     P = 8
     w = wl.all_to_all_tokens(device="cuda")
     xs = w.inputs
@@ -131,7 +132,7 @@ def test_config4a_all_to_all_bf16_P8_full(dt, wl):
         assert_same(host(outs[j].reshape(-1)[idx]), want[j], f"rank {j}")
 
 
-def test_config4b_uneven_all_gather_i32_P8_full(dt, wl):
+def test_full_uneven_all_gather_i32_P8_rows16384(dt, wl):
     P = 8
     w = wl.uneven_gather(device="cuda")
     rows, cols = w.meta["rows"], w.meta["cols"]
@@ -149,7 +150,7 @@ def test_config4b_uneven_all_gather_i32_P8_full(dt, wl):
         assert torch.equal(per[q], shared), f"rank {q}"
 
 
-# ----------------------------------------------------------------- config 5
+# ------------------------------------------- size sweep 4 KiB .. 1 GiB per rank
 SWEEP_SMALL = [4096, 1 << 20]
 
 

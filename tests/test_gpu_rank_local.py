@@ -174,3 +174,20 @@ def test_rank_local_missing_rank_times_out_and_reset_recovers(dt):
         assert errs == [None] * P, errs
         torch.cuda.synchronize()
         assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, 1))
+
+
+def test_native_thread_driver_runs_the_rank_local_step():
+    # rank_local_step (built with the library) runs the barrier / ReduceScatter /
+    # barrier / AllGather step from one std::thread per rank through the C ABI;
+    # here at a small ragged size, P=3, with a clean group status at the end.
+    import json
+    import os
+    import subprocess
+    tool = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "same_device_collective_gb300", "rank_local_step")
+    res = subprocess.run([tool, "3", "96", "72", "50"], capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stdout + res.stderr
+    out = json.loads(res.stdout.strip().splitlines()[-1])
+    assert out["status_ok"] is True and out["P"] == 3 and out["steps"] == 50
+    bad = subprocess.run([tool, "3", "97", "72", "5"], capture_output=True, text=True, timeout=60)
+    assert bad.returncode != 0 and "error" in json.loads(bad.stdout.strip().splitlines()[-1])
