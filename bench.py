@@ -546,6 +546,13 @@ def measure_rows(dt, dev, peak, only=None):
                          20, reps=STEADY_REPS)
         rec("all_gather_into_vec_bf16_P4_2048x4096", (P + P * P) * (R // P) * C * 2, ms)
         del vec
+        # the plain AllGather of the same shards, timed the same way (in the
+        # bench step it reads its input from L2; here, as above, from HBM)
+        ag = [torch.empty(R, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ms = time_events(lambda: dt.dt_all_gather(g, ALL, shards, ag, None, R // P, C * 2), 20,
+                         reps=STEADY_REPS)
+        rec("all_gather_bf16_P4_2048x4096", (P + P * P) * (R // P) * C * 2, ms)
+        del ag
         rsb = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
         ms = time_events(lambda: dt.dt_reduce_scatter(g, ALL, full, rsb, R // P * C, "bf16",
                                                       "sum_stepwise"), 20, reps=STEADY_REPS)

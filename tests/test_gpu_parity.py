@@ -421,5 +421,15 @@ def test_invalid_arguments_are_rejected_without_launch(dt):
         dt.dt_all_to_all(g, dt.DT_ALL_RANKS, x, o, 0)
         dt.dt_reduce_scatter(g, dt.DT_ALL_RANKS, x, o, 0, "f32", "sum")
         dt.dt_all_gather(g, dt.DT_ALL_RANKS, x, o, [0, 0, 0], 0, 4)
+        for t in o:
+            t.fill_(-7.25)               # canary: nothing below may write
+        vec = [torch.full((16,), -7.25, device="cuda") for _ in range(P * P)]
+        dt.dt_bucket_allreduce(g, [o, x], [0, 0], "f32", "avg")
+        dt.dt_replicate_to_shard(g, dt.DT_ALL_RANKS, x, o, None, 0, 16)
+        dt.dt_all_gather_into_vec(g, dt.DT_ALL_RANKS, x, vec, None, 0, 16)
+        dt.dt_all_to_all_2d(g, dt.DT_ALL_RANKS, x, o, 0, 12, 4, 0, 1)
+        dt.dt_all_to_all_2d(g, dt.DT_ALL_RANKS, x, o, 6, 0, 4, 1, 0)
         assert dt.dt_launch_count() == n0
+        torch.cuda.synchronize()
+        assert all(bool((t == -7.25).all()) for t in o + vec)
         assert dt.dt_group_check(g) == dt.DT_OK
