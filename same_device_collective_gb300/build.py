@@ -30,6 +30,11 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # explicitly rounded adds, divides and multiplies; this keeps it that way).
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]
+# DT_NVTX=1: every public entry point opens an NVTX range (profiler timelines);
+# its objects live in their own folder so the two flavours never mix.
+if os.environ.get("DT_NVTX") == "1":
+    NVFLAGS.append("-DDT_NVTX")
+    BUILD = BUILD + "_nvtx"
 
 
 def nvcc() -> str:
@@ -72,7 +77,9 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             os.remove(os.path.join(BUILD, f))
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    if force or _stale(LIB, objs):
+    stamp = LIB + ".objs"            # the objects the library was last linked from
+    linked = open(stamp).read() if os.path.exists(stamp) else ""
+    if force or _stale(LIB, objs) or linked != "\n".join(objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
                "-lpthread", "-ldl", "-lrt"]
@@ -80,6 +87,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp, "w") as f:
+            f.write("\n".join(objs))
     tool_src = os.path.join(CSRC, "rank_local_step.cpp")
     if force or _stale(STEP_TOOL, [tool_src, LIB, os.path.join(INCLUDE, "dt.h")]):
         tmp = STEP_TOOL + f".tmp{os.getpid()}"

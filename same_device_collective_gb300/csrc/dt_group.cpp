@@ -9,18 +9,38 @@
 // the caller passes are the store's slots, they travel to the device as the
 // kernel's parameter block (or, for buckets, as a table staged in HBM), and
 // ordering is the order of the caller's stream.
+#include <cxxabi.h>
+
 #include <algorithm>
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <new>
+#include <string>
 #include <thread>
+#include <tuple>
 #include <unordered_map>
 #include <utility>
 #include <vector>
 
 #include "dt_group.h"
+
+// Built with -DDT_NVTX (DT_NVTX=1 when building), every public entry point
+// opens an NVTX range named after itself for profiler timelines.
+#ifdef DT_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+#define DT_TRACE() NvtxRange dt_nvtx_range_(__func__)
+#else
+#define DT_TRACE() ((void)0)
+#endif
 
 namespace dt {
 
@@ -35,6 +55,34 @@ bool pdl_enabled()
         return !(env && env[0] == '0');
     }();
     return on;
+}
+
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char *env = std::getenv("DT_LOG");
+        return env && env[0] && env[0] != '0';
+    }();
+    return on;
+}
+
+void log_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool cooperative,
+                cudaError_t result)
+{
+    const char *mangled = nullptr;
+    std::string name = "?";
+    if (cudaFuncGetName(&mangled, fn) == cudaSuccess && mangled) {
+        int status = 0;
+        char *d = abi::__cxa_demangle(mangled, nullptr, nullptr, &status);
+        name = (status == 0 && d) ? d : mangled;
+        std::free(d);
+    }
+    std::fprintf(stderr,
+                 "dt: launch %s grid=(%u,%u,%u) block=(%u,%u,%u) smem=%zu stream=%p pdl=%d "
+                 "cooperative=%d -> %s\n",
+                 name.c_str(), grid.x, grid.y, grid.z, block.x, block.y, block.z, smem,
+                 static_cast<void *>(s), pdl_enabled() ? 1 : 0, cooperative ? 1 : 0,
+                 cudaGetErrorName(result));
 }
 
 int sm_count(int device)
@@ -54,9 +102,8 @@ int sm_count(int device)
 cudaError_t resident_blocks(const void *fn, int threads, int device, int *out, size_t dyn_smem)
 {
     static std::mutex mu;
-    static std::unordered_map<uint64_t, int> cache;
-    const uint64_t key = reinterpret_cast<uintptr_t>(fn) * 131u + (uint64_t)device * 7u + threads +
-                         (uint64_t)dyn_smem * 1000003u;
+    static std::map<std::tuple<const void *, int, int, size_t>, int> cache;
+    const auto key = std::make_tuple(fn, device, threads, dyn_smem);
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -414,6 +461,7 @@ uint64_t dt_launch_count(void) { return dt::g_launches.load(std::memory_order_re
 
 dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
 {
+    DT_TRACE();
     if (!out) return DT_ERR_INVALID;
     *out = nullptr;
     if (world_size < 1 || world_size > DT_MAX_RANKS || cuda_device < 0) return DT_ERR_INVALID;
@@ -462,6 +510,7 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
 
 dt_status dt_group_destroy(dt_group_t g)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     DeviceScope scope(g->device);
     for (int k = 0; k < dt_group::kPlanSlots; ++k)
@@ -473,6 +522,7 @@ dt_status dt_group_destroy(dt_group_t g)
 
 dt_status dt_group_reset(dt_group_t g, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g->mu);
     DeviceScope scope(g->device);
@@ -544,6 +594,7 @@ dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_byt
 dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *const *out,
                        size_t count, int dtype, int op, unsigned flags, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out) return DT_ERR_INVALID;
@@ -608,6 +659,7 @@ dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *cons
 dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void *const *out,
                             size_t recv_count, int dtype, int op, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out) return DT_ERR_INVALID;
@@ -664,6 +716,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
                         const size_t *rows, size_t rows_equal, size_t row_bytes, unsigned flags,
                         void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         // a rank passes its own shard: rows must be NULL, rows_equal its row count
@@ -733,6 +786,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
 dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *const *out,
                         size_t chunk_bytes, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out) return DT_ERR_INVALID;
@@ -789,6 +843,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
                               size_t n_tensors, int dtype, int op, size_t bucket_cap_bytes,
                               void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
@@ -896,10 +951,18 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         }
         e = cudaMemcpyAsync(g->d_plan[k], h, plan_bytes, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_status(e);
+        if (dt::log_enabled()) {
+            std::string blocks;
+            for (const dt_group::PlanLaunch &L : bl) blocks += (blocks.empty() ? "" : ",") + std::to_string(L.blocks);
+            std::fprintf(stderr, "dt: bucket plan in slot %d: %zu tensors x %d ranks, %zu buckets, blocks [%s]\n",
+                         k, n_tensors, P, bl.size(), blocks.c_str());
+        }
         g->plan_key[k] = std::move(key);
         g->plan_launches[k] = std::move(bl);
         g->plan_ptr_bytes[k] = ptr_bytes;
         g->plan_tab_bytes[k] = tab_bytes;
+    } else if (dt::log_enabled()) {
+        std::fprintf(stderr, "dt: bucket plan in slot %d reused\n", k);
     }
 
     const unsigned char *d = static_cast<const unsigned char *>(g->d_plan[k]);
@@ -932,6 +995,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
 dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, void *const *out,
                                 const int *shard_idx, size_t rows, size_t row_bytes, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out) return DT_ERR_INVALID;
@@ -987,6 +1051,7 @@ dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, 
                                  const size_t *rows, size_t rows_equal, size_t row_bytes,
                                  void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out || rows) return DT_ERR_INVALID;
@@ -1055,6 +1120,7 @@ dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *
                            size_t R, size_t C, size_t elem_bytes, int src_dim, int dest_dim,
                            void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS) {
         if (!in || !out) return DT_ERR_INVALID;
@@ -1124,6 +1190,7 @@ dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *
 
 dt_status dt_barrier(dt_group_t g, int rank, void *stream)
 {
+    DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     if (rank != DT_ALL_RANKS)
         return rank_local(g, rank, make_call(CK_BARRIER, nullptr, nullptr, 0, 0, 0, 0, 0, stream));
@@ -1138,6 +1205,7 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream)
 
 dt_status dt_async_begin(dt_group_t g, void *stream, void **comm_stream)
 {
+    DT_TRACE();
     if (!g || !comm_stream) return DT_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g->mu);
     dt_status st = take_device_error(g);
@@ -1156,6 +1224,7 @@ dt_status dt_async_begin(dt_group_t g, void *stream, void **comm_stream)
 
 dt_status dt_async_end(dt_group_t g, dt_work_t *work)
 {
+    DT_TRACE();
     if (!g || !work) return DT_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g->mu);
     if (!g->scope_open) return DT_ERR_INVALID;
@@ -1188,6 +1257,7 @@ dt_status dt_async_end(dt_group_t g, dt_work_t *work)
 
 dt_status dt_work_wait(dt_work_t w, void *stream)
 {
+    DT_TRACE();
     if (!w || !w->g) return DT_ERR_INVALID;
     DeviceScope scope(w->g->device);
     if (!scope.ok) return DT_ERR_CUDA;

@@ -154,6 +154,12 @@ void count_launch();
 // default; the environment variable DT_PDL=0 turns it off.
 bool pdl_enabled();
 
+// DT_LOG=1 in the environment: every launch prints its kernel, grid, block,
+// dynamic shared memory, stream and launch attributes to stderr.
+bool log_enabled();
+void log_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool cooperative,
+                cudaError_t result);
+
 template <typename... Params, typename... Args>
 cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t s, bool cooperative, Args &&...args)
@@ -178,7 +184,9 @@ cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attrs;
     cfg.numAttrs = n;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
+    if (log_enabled()) log_launch(reinterpret_cast<const void *>(fn), grid, block, smem, s, cooperative, e);
+    return e;
 }
 int sm_count(int device);
 // SMs x blocks of `fn` one SM holds at once (cached per kernel and device).

@@ -93,3 +93,18 @@ def test_pointer_table_marshals_tensors_and_addresses(dt):
             dt.dt_bucket_allreduce(None, arg, [4, 1], "f32", "sum", stream=0)
         lib_status.append(e.value.status)
     assert lib_status == [dt.DT_ERR_INVALID] * 2
+
+
+def test_nvtx_flavour_compiles(tmp_path):
+    # DT_NVTX=1 builds wrap every entry point in an NVTX range; the host
+    # translation unit must compile that way too (compiled to a scratch
+    # object here, so the in-tree library is left as it is).
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    from same_device_collective_gb300 import build as b
+    cmd = [b.nvcc(), *b.ARCH, "-O1", "-std=c++17", "-Xcompiler", "-fPIC", "-DDT_NVTX",
+           "-I", os.path.join(root, "include"), "-I", b.CSRC, "-c",
+           os.path.join(b.CSRC, "dt_group.cpp"), "-o", str(tmp_path / "g.o")]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
