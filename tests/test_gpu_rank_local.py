@@ -191,3 +191,60 @@ def test_native_thread_driver_runs_the_rank_local_step():
     assert out["status_ok"] is True and out["P"] == 3 and out["steps"] == 50
     bad = subprocess.run([tool, "3", "97", "72", "5"], capture_output=True, text=True, timeout=60)
     assert bad.returncode != 0 and "error" in json.loads(bad.stdout.strip().splitlines()[-1])
+
+
+@pytest.mark.parametrize("P", [3, 8])
+def test_rank_local_chained_rounds_stay_ordered(dt, P):
+    # P threads run the same seeded sequence of 120 rounds.  Each round first
+    # updates the rank's buffer on its own stream (b = 0.5 b + (k + r)), then
+    # makes one rank-local call on it: an in-place AllReduce, a ReduceScatter
+    # (avg) followed by an AllGather back into b, an AllToAll copied back into
+    # b, or a bare barrier.  Every input depends on the previous collective's
+    # output, so an ordering slip anywhere shows in the final buffers, which a
+    # host replica built from the oracle must match bit for bit.
+    K, n = 120, 24_024
+    m = n // P
+    rng = np.random.default_rng(P)
+    kinds = rng.choice(["ar", "rs_ag", "a2a", "barrier"], size=K, p=[0.35, 0.3, 0.2, 0.15])
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    bufs = [torch.arange(n, dtype=torch.float32, device="cuda") * (r + 1) / n for r in range(P)]
+    host_b = [host(b).copy() for b in bufs]
+    torch.cuda.synchronize()
+    with group(P) as g:
+        def rank(r):
+            s = streams[r]
+            b = bufs[r]
+            shard = torch.empty(m, device="cuda")
+            tmp = torch.empty(n, device="cuda")
+            with torch.cuda.stream(s):
+                for k, kind in enumerate(kinds):
+                    b.mul_(0.5).add_(float(k + r))
+                    if kind == "ar":
+                        dt.dt_allreduce(g, r, [b], [b], n, "f32", "sum", 0, s)
+                    elif kind == "rs_ag":
+                        dt.dt_reduce_scatter(g, r, [b], [shard], m, "f32", "avg", s)
+                        dt.dt_all_gather(g, r, [shard], [b], None, m, 4 * 1, 0, s)
+                    elif kind == "a2a":
+                        dt.dt_all_to_all(g, r, [b], [tmp], m * 4, s)
+                        b.copy_(tmp)
+                    else:
+                        dt.dt_barrier(g, r, s)
+        errs = run_ranks(P, rank)
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+        win = dt.dt_debug_read_window(g)
+    for k, kind in enumerate(kinds):
+        host_b = [(hb * np.float32(0.5)).astype(np.float32) + np.float32(k + r)
+                  for r, hb in enumerate(host_b)]
+        host_b = [hb.astype(np.float32) for hb in host_b]
+        if kind == "ar":
+            host_b = oracle.allreduce("f32", "sum", host_b)
+        elif kind == "rs_ag":
+            rs = oracle.reduce_scatter("f32", "avg", host_b)
+            host_b = [g.view(np.float32) for g in oracle.all_gather(rs, [m] * P, 4)]
+        elif kind == "a2a":
+            host_b = [a.view(np.float32) for a in oracle.all_to_all(host_b)]
+    for r in range(P):
+        assert_same(host(bufs[r]), host_b[r], f"rank {r}")
+    assert np.array_equal(win, oracle.expected_window(P, int((kinds == "barrier").sum())))
