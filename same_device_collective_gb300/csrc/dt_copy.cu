@@ -44,15 +44,23 @@ __device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
 // and returns.
 constexpr int kBulkThreads = 32;
 
-// Tile size and pipeline depth per launch layout (measured on GB300): the
-// P^2 single-destination segments of an AllToAll stream best as 16 KiB tiles
-// 12 deep; gathers (few segments, several destinations each) as 32 KiB x 6.
+// Tile size and pipeline depth, measured on GB300 per launch layout:
+//   kStream: the P^2 single-destination segments of an AllToAll stream best
+//            as 16 KiB tiles 12 deep;
+//   kGather: few segments (equal or uneven shards, shared or per-rank
+//            outputs of moderate size, row-block copies): 32 KiB x 6;
+//   kWide:   large launches whose segments each store to 2..8 destinations
+//            (per-rank gathers): every tile is stored several times, so each
+//            stage stays busy long enough that two 96 KiB stages beat more,
+//            smaller ones (the RS+AG step 105.1 -> 104.2 us).
 // Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
 // bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
-template <int NSEG>
+enum BulkKind { kStream = 0, kGather = 1, kWide = 2 };
+
+template <int KIND>
 struct BulkShape {
-    static constexpr int kStages = NSEG > DT_MAX_RANKS ? 12 : 6;
-    static constexpr int kTile = NSEG > DT_MAX_RANKS ? 16384 : 32768;
+    static constexpr int kStages = KIND == kStream ? 12 : KIND == kGather ? 6 : 2;
+    static constexpr int kTile = KIND == kStream ? 16384 : KIND == kGather ? 32768 : 98304;
     static constexpr size_t kBarBytes = ((size_t)kStages * 8 + 127) / 128 * 128;
     static constexpr size_t kSmem = kBarBytes + (size_t)kStages * kTile;
     static_assert(kBarBytes >= (size_t)kStages * 8, "mbarrier area too small");
@@ -60,12 +68,12 @@ struct BulkShape {
     static_assert(kSmem <= 227 * 1024, "bulk copy shared memory above the per-block limit");
 };
 
-template <int NSEG, int NOUT>
+template <int NSEG, int NOUT, int KIND>
 __global__ void __launch_bounds__(kBulkThreads)
 copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
-    constexpr int kBulkStages = BulkShape<NSEG>::kStages;
-    constexpr int kBulkTile = BulkShape<NSEG>::kTile;
+    constexpr int kBulkStages = BulkShape<KIND>::kStages;
+    constexpr int kBulkTile = BulkShape<KIND>::kTile;
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_begin();
     if (threadIdx.x != 0) return;
@@ -73,7 +81,7 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     if (first >= p.total_tiles) return;
     const uint64_t n = (p.total_tiles - first + step - 1) / step;   // tiles of this block
     const uint32_t bar0 = smem_addr(smem);
-    const uint32_t buf0 = smem_addr(smem + BulkShape<NSEG>::kBarBytes);
+    const uint32_t buf0 = smem_addr(smem + BulkShape<KIND>::kBarBytes);
     for (int k = 0; k < kBulkStages; ++k) mbar_init(bar0 + 8 * k, 1);
     mbar_init_fence();
     const uint64_t pol = policy_evict_first();
@@ -138,6 +146,41 @@ copy_byte_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     }
 }
 
+template <int NSEG, int NOUT, int KIND>
+cudaError_t launch_bulk(const CopyParams<NSEG, NOUT> &p, int device, cudaStream_t s)
+{
+    using Shape = BulkShape<KIND>;
+    void (*fn)(CopyParams<NSEG, NOUT>) = copy_bulk_kernel<NSEG, NOUT, KIND>;
+    static bool attr_set = false;   // per instantiation; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Shape::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int resident = 0;
+    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
+                                    &resident, Shape::kSmem);
+    if (e != cudaSuccess) return e;
+    const uint64_t gx = p.total_tiles < (uint64_t)resident ? p.total_tiles : (uint64_t)resident;
+    return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), Shape::kSmem, s, false, p);
+}
+
+// Tiles of tile_bytes covering the used segments; records each segment's first tile.
+template <int NSEG, int NOUT>
+uint64_t cut_tiles(CopyParams<NSEG, NOUT> &p, uint64_t tile_bytes)
+{
+    p.tile_bytes = tile_bytes;
+    uint64_t tiles = 0;
+    for (int i = 0; i < p.nseg; ++i) {
+        p.seg[i].tile_begin = tiles;
+        tiles += (p.seg[i].bytes + tile_bytes - 1) / tile_bytes;
+    }
+    p.total_tiles = tiles;
+    return tiles;
+}
+
 template <int NSEG, int NOUT>
 cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
                      const ErrorSink &sink, int device, cudaStream_t s)
@@ -146,44 +189,38 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
     memset(&p, 0, sizeof p);
     for (int r = 0; r < nout && r < NOUT; ++r) p.out[r] = out[r];
     p.sink = sink;
-    p.tile_bytes = vec ? (uint64_t)BulkShape<NSEG>::kTile : 4096;
-    uint64_t tiles = 0;
+    int max_dst = 0;                    // most destinations of any segment
     int used = 0;
     for (int i = 0; i < nseg; ++i) {
         if (segs[i].bytes == 0 || segs[i].dst_count == 0) continue;
-        p.seg[used] = segs[i];
-        p.seg[used].tile_begin = tiles;
-        tiles += (segs[i].bytes + p.tile_bytes - 1) / p.tile_bytes;
-        ++used;
+        p.seg[used++] = segs[i];
+        if (segs[i].dst_count > max_dst) max_dst = segs[i].dst_count;
     }
     if (used == 0) return cudaSuccess;   // nothing to move
     p.nseg = used;
-    p.total_tiles = tiles;
 
-    if (vec) {
-        void (*fn)(CopyParams<NSEG, NOUT>) = copy_bulk_kernel<NSEG, NOUT>;
-        static bool attr_set = false;   // per instantiation; the attribute is per function
-        if (!attr_set) {
-            cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)BulkShape<NSEG>::kSmem);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
+    if (!vec) {
+        const uint64_t tiles = cut_tiles(p, 4096);
+        void (*fn)(CopyParams<NSEG, NOUT>) = copy_byte_kernel<NSEG, NOUT>;
         int resident = 0;
-        cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
-                                        &resident, BulkShape<NSEG>::kSmem);
+        cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
         if (e != cudaSuccess) return e;
         const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
-        return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), BulkShape<NSEG>::kSmem, s,
-                             false, p);
+        return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
     }
-    void (*fn)(CopyParams<NSEG, NOUT>) = copy_byte_kernel<NSEG, NOUT>;
-    int resident = 0;
-    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
-    if (e != cudaSuccess) return e;
-    const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
-    return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
+    // Wide tiles need enough of them to keep every SM busy to the end (at
+    // least 4 per SM; at 2 per SM a 16 MiB-per-rank P=2 gather lost 17%), and
+    // they stop paying at 16 destinations, where each tile carries 1.5 MiB of
+    // stores and the last wave runs half empty.
+    if (max_dst > 1 && max_dst <= 8 &&
+        cut_tiles(p, BulkShape<kWide>::kTile) >= 4 * (uint64_t)sm_count(device))
+        return launch_bulk<NSEG, NOUT, kWide>(p, device, s);
+    if (NSEG > DT_MAX_RANKS) {
+        cut_tiles(p, BulkShape<kStream>::kTile);
+        return launch_bulk<NSEG, NOUT, kStream>(p, device, s);
+    }
+    cut_tiles(p, BulkShape<kGather>::kTile);
+    return launch_bulk<NSEG, NOUT, kGather>(p, device, s);
 }
 
 }  // namespace
