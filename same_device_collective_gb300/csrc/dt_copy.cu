@@ -5,7 +5,8 @@
 // the shard's row offset, AllToAll sends chunk j of rank i to rank j.  The
 // host turns a call into a list of segments (source range -> one or more
 // destinations at one offset); one launch moves them all.  Each segment is
-// cut into tiles and a resident grid strides over the tiles of all segments.
+// cut into tiles and the grid (one to eight waves of blocks, see bulk_grid)
+// strides over the tiles of all segments.
 //
 // 16-byte-aligned segments go through the copy engine (TMA bulk copies): a
 // tile is loaded from HBM into shared memory once and stored from there to
@@ -56,6 +57,23 @@ constexpr int kBulkThreads = 32;
 // Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
 // bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
 enum BulkKind { kStream = 0, kGather = 1, kWide = 2 };
+
+// Blocks per launch.  One block per SM holds a shape's stages; extra blocks
+// run in later waves, and the hardware hands each to whichever SM frees up
+// first, so SMs that stream slower take fewer tiles.  That balancing pays
+// when tiles are plentiful (16+ per SM: 8 waves; the uneven 8-rank gather
+// +8%, its shared-output form +6%) and for the wide shape's few large tiles
+// (4 waves: the RS+AG step 100.7 -> 98.7 us), but restarting the pipeline
+// costs more than it saves for a few thousand small tiles served from L2
+// (ReplicateToShard -14% at 4 waves) and for the AllToAll (-1%).
+template <int KIND>
+uint64_t bulk_grid(uint64_t tiles, int resident)
+{
+    const bool plenty = tiles >= 16 * (uint64_t)resident;
+    const uint64_t waves = KIND == kStream ? 1 : plenty ? 8 : KIND == kWide ? 4 : 1;
+    const uint64_t cap = (uint64_t)resident * waves;
+    return tiles < cap ? tiles : cap;
+}
 
 template <int KIND>
 struct BulkShape {
@@ -163,7 +181,7 @@ cudaError_t launch_bulk(const CopyParams<NSEG, NOUT> &p, int device, cudaStream_
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
                                     &resident, Shape::kSmem);
     if (e != cudaSuccess) return e;
-    const uint64_t gx = p.total_tiles < (uint64_t)resident ? p.total_tiles : (uint64_t)resident;
+    const uint64_t gx = bulk_grid<KIND>(p.total_tiles, resident);
     return launch_kernel(fn, dim3((unsigned)gx), dim3(kBulkThreads), Shape::kSmem, s, false, p);
 }
 
