@@ -226,3 +226,26 @@ def test_placement_conversions_write_only_their_outputs(dt):
     for j, o in enumerate(a2a):
         assert o.intact(), f"all-to-all rank {j}"
         assert_same(host(o.view(torch.int32)), want_a2a[j], f"all-to-all rank {j}")
+
+
+@pytest.mark.parametrize("rows,shared", [([8193, 8190], False), ([3073, 3070], True)])
+def test_large_gathers_in_waves_write_only_their_outputs(dt, rows, shared):
+    # Big enough for the bulk copy's multi-wave grids: per-rank outputs of two
+    # ~128 MiB shards take 96 KiB tiles in 8 waves, a shared output of two
+    # ~48 MiB shards 32 KiB tiles in 8 waves; both shards end in a partial tile.
+    P, row_bytes = 2, 16384
+    gen = torch.Generator(device="cuda").manual_seed(sum(rows))
+    xs = [torch.randint(0, 256, (c * row_bytes,), generator=gen, device="cuda", dtype=torch.uint8)
+          for c in rows]
+    total = sum(rows) * row_bytes
+    # 16-byte-aligned outputs: the bulk-copy path (a misaligned one takes the byte kernel)
+    outs = [Guarded(total)] if shared else [Guarded(total) for _ in range(P)]
+    with group(P) as g:
+        dt.dt_all_gather(g, dt.DT_ALL_RANKS, xs, [o.view(torch.uint8) for o in outs] * (P if shared else 1),
+                         rows, 0, row_bytes, flags=dt.DT_SHARED_OUTPUT if shared else 0)
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    want = torch.cat(xs)
+    for q, o in enumerate(outs):
+        assert o.intact(), f"output {q}"
+        assert torch.equal(o.view(torch.uint8), want), f"output {q}"
