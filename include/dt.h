@@ -127,7 +127,9 @@ dt_status dt_group_reset(dt_group_t g, void *stream);
 dt_status dt_group_check(dt_group_t g);
 dt_status dt_group_error_detail(dt_group_t g, int *rank, int *peer, int *generation);
 
-/* Number of ranks; number of barriers issued since create/reset. */
+/* Number of ranks; number of barrier launches issued on the host since
+ * create/reset (a barrier captured in a CUDA graph counts once, however
+ * often the graph replays; the device-side generations live in the window). */
 int dt_group_size(dt_group_t g);
 int64_t dt_group_generation(dt_group_t g);
 
@@ -138,6 +140,17 @@ const char *dt_status_string(dt_status st);
 
 /* Kernels this library has launched in this process (all groups). */
 uint64_t dt_launch_count(void);
+
+/* CUDA graphs: group-wide calls may be captured in a stream capture.  Every
+ * collective passes its rank pointers in the kernel's parameter block, and the
+ * barrier keeps each rank's generation on the device, so replays advance the
+ * window as eager calls would.  Make one eager call of each collective before
+ * capturing it (the first call sets kernel attributes and caches launch
+ * shapes).  A bucket all-reduce captured while its plan is cached (the same
+ * gradients, counts, dtype, op and cap as an earlier call) replays against
+ * that plan; the group holds two plans, so a bucket call with other arguments
+ * can replace it, after which the graph must be captured again.  Rank-local
+ * calls meet on the host and are not meant for capture. */
 
 /* ------------------------------------------------------------- collectives */
 
