@@ -146,11 +146,13 @@ uint64_t dt_launch_count(void);
  * barrier keeps each rank's generation on the device, so replays advance the
  * window as eager calls would.  Make one eager call of each collective before
  * capturing it (the first call sets kernel attributes and caches launch
- * shapes).  A bucket all-reduce captured while its plan is cached (the same
- * gradients, counts, dtype, op and cap as an earlier call) replays against
- * that plan; the group holds two plans, so a bucket call with other arguments
- * can replace it, after which the graph must be captured again.  Rank-local
- * calls meet on the host and are not meant for capture. */
+ * shapes).  A bucket all-reduce can be captured only after an eager call with
+ * the same gradients, counts, dtype, op and cap (building a plan may allocate;
+ * otherwise the call returns DT_ERR_UNSUPPORTED).  The captured call pins that
+ * plan in the group: later bucket calls with other arguments use other plan
+ * slots, so the graph keeps replaying against its own plan.  The group must
+ * outlive every graph that holds its calls.  Rank-local calls meet on the host
+ * and are not meant for capture. */
 
 /* ------------------------------------------------------------- collectives */
 

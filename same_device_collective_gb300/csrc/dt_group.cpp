@@ -212,20 +212,20 @@ dt_status issue_barrier(dt_group *g, cudaStream_t s)
     return DT_OK;
 }
 
-void release_plan_slot(dt_group *g, int k)
+void release_plan_slot(dt_group::PlanSlot &sl)
 {
-    if (g->h_plan[k]) cudaFreeHost(g->h_plan[k]);
-    if (g->d_plan[k]) cudaFree(g->d_plan[k]);
-    g->h_plan[k] = nullptr;
-    g->d_plan[k] = nullptr;
-    g->plan_bytes[k] = 0;
+    if (sl.h) cudaFreeHost(sl.h);
+    if (sl.d) cudaFree(sl.d);
+    sl.h = nullptr;
+    sl.d = nullptr;
+    sl.bytes = 0;
 }
 
 void destroy_all(dt_group *g)
 {
-    for (int k = 0; k < dt_group::kPlanSlots; ++k) {
-        release_plan_slot(g, k);
-        if (g->plan_done[k]) cudaEventDestroy(g->plan_done[k]);
+    for (dt_group::PlanSlot &sl : g->plans) {
+        release_plan_slot(sl);
+        if (sl.done) cudaEventDestroy(sl.done);
     }
     for (dt_work *w : g->work_all) {
         if (w->end) cudaEventDestroy(w->end);
@@ -243,17 +243,24 @@ void destroy_all(dt_group *g)
     delete g;
 }
 
-cudaError_t grow_plan_slot(dt_group *g, int k, size_t bytes)
+cudaError_t grow_plan_slot(dt_group::PlanSlot &sl, size_t bytes)
 {
-    if (bytes <= g->plan_bytes[k]) return cudaSuccess;
-    size_t cap = g->plan_bytes[k] ? g->plan_bytes[k] : ((size_t)1 << 20);
+    if (bytes <= sl.bytes) return cudaSuccess;
+    size_t cap = sl.bytes ? sl.bytes : ((size_t)1 << 20);
     while (cap < bytes) cap *= 2;
-    release_plan_slot(g, k);
-    cudaError_t e = cudaHostAlloc(&g->h_plan[k], cap, cudaHostAllocDefault);
-    if (e == cudaSuccess) e = cudaMalloc(&g->d_plan[k], cap);
-    if (e != cudaSuccess) { release_plan_slot(g, k); return e; }
-    g->plan_bytes[k] = cap;
+    release_plan_slot(sl);
+    cudaError_t e = cudaHostAlloc(&sl.h, cap, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaMalloc(&sl.d, cap);
+    if (e != cudaSuccess) { release_plan_slot(sl); return e; }
+    sl.bytes = cap;
     return cudaSuccess;
+}
+
+// A new, empty plan slot (its buffers grow on first use).
+cudaError_t add_plan_slot(dt_group *g)
+{
+    g->plans.emplace_back();
+    return cudaEventCreateWithFlags(&g->plans.back().done, cudaEventDisableTiming);
 }
 
 // Greedy bucket plan shared by dt_bucket_plan and dt_bucket_allreduce.
@@ -490,8 +497,8 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
         e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&g->h_err_dev), g->h_err, 0);
     }
     for (int k = 0; k < dt_group::kPlanSlots && e == cudaSuccess; ++k) {
-        e = cudaEventCreateWithFlags(&g->plan_done[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = grow_plan_slot(g, k, (size_t)1 << 20);
+        e = add_plan_slot(g);
+        if (e == cudaSuccess) e = grow_plan_slot(g->plans.back(), (size_t)1 << 20);
     }
     for (int r = 0; r < world_size && e == cudaSuccess; ++r)
         e = cudaEventCreateWithFlags(&g->rv_ready[r], cudaEventDisableTiming);
@@ -513,8 +520,8 @@ dt_status dt_group_destroy(dt_group_t g)
     DT_TRACE();
     if (!g) return DT_ERR_INVALID;
     DeviceScope scope(g->device);
-    for (int k = 0; k < dt_group::kPlanSlots; ++k)
-        if (g->plan_used[k]) cudaEventSynchronize(g->plan_done[k]);
+    for (dt_group::PlanSlot &sl : g->plans)
+        if (sl.used) cudaEventSynchronize(sl.done);
     cudaDeviceSynchronize();
     destroy_all(g);
     return DT_OK;
@@ -867,14 +874,22 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     for (size_t i = 0; i < n_tensors * P; ++i) key.push_back((uint64_t)(uintptr_t)grads[i]);
 
     int k = -1;
-    for (int j = 0; j < dt_group::kPlanSlots; ++j)
-        if (g->plan_used[j] && g->plan_key[j] == key) k = j;
+    for (size_t j = 0; j < g->plans.size(); ++j)
+        if (g->plans[j].used && g->plans[j].key == key) k = (int)j;
 
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) return DT_ERR_CUDA;
+    const bool capturing = capture != cudaStreamCaptureStatusNone;
 
+    if (k < 0 && capturing) {
+        // building a plan may allocate, which a capture forbids: the call must
+        // follow an eager call with the same arguments
+        return DT_ERR_UNSUPPORTED;
+    }
     if (k < 0) {
         // validate and find overlapping gradient buffers (sorted sweep)
         std::vector<Range> ranges;
@@ -919,14 +934,25 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         const size_t ptr_bytes = n_tensors * P * sizeof(void *);
         const size_t tab_bytes = n_tensors * sizeof(dt::BucketTensor);
         const size_t plan_bytes = ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t);
-        k = g->next_plan;
-        g->next_plan = (k + 1) % dt_group::kPlanSlots;
-        if (g->plan_used[k]) e = cudaEventSynchronize(g->plan_done[k]);
-        g->plan_key[k].clear();   // the slot no longer holds a valid plan
-        if (e == cudaSuccess) e = grow_plan_slot(g, k, plan_bytes);
+        // the next unpinned slot, round robin; a new one when all are pinned
+        const int nslots = (int)g->plans.size();
+        for (int i = 0; i < nslots && k < 0; ++i) {
+            const int j = (g->next_plan + i) % nslots;
+            if (!g->plans[j].pinned) k = j;
+        }
+        if (k < 0) {
+            e = add_plan_slot(g);
+            if (e != cudaSuccess) return cuda_status(e);
+            k = (int)g->plans.size() - 1;
+        }
+        g->next_plan = (k + 1) % (int)g->plans.size();
+        dt_group::PlanSlot &sl = g->plans[k];
+        if (sl.used) e = cudaEventSynchronize(sl.done);
+        sl.key.clear();   // the slot no longer holds a valid plan
+        if (e == cudaSuccess) e = grow_plan_slot(sl, plan_bytes);
         if (e != cudaSuccess) return cuda_status(e);
 
-        unsigned char *h = static_cast<unsigned char *>(g->h_plan[k]);
+        unsigned char *h = static_cast<unsigned char *>(sl.h);
         memcpy(h, grads, ptr_bytes);
         dt::BucketTensor *tab = reinterpret_cast<dt::BucketTensor *>(h + ptr_bytes);
         uint32_t *starts = reinterpret_cast<uint32_t *>(h + ptr_bytes + tab_bytes);
@@ -949,7 +975,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
                 starts[L.start_off + j] = (uint32_t)(t - L.tb);
             }
         }
-        e = cudaMemcpyAsync(g->d_plan[k], h, plan_bytes, cudaMemcpyHostToDevice, s);
+        e = cudaMemcpyAsync(sl.d, h, plan_bytes, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_status(e);
         if (dt::log_enabled()) {
             std::string blocks;
@@ -957,17 +983,20 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
             std::fprintf(stderr, "dt: bucket plan in slot %d: %zu tensors x %d ranks, %zu buckets, blocks [%s]\n",
                          k, n_tensors, P, bl.size(), blocks.c_str());
         }
-        g->plan_key[k] = std::move(key);
-        g->plan_launches[k] = std::move(bl);
-        g->plan_ptr_bytes[k] = ptr_bytes;
-        g->plan_tab_bytes[k] = tab_bytes;
+        sl.key = std::move(key);
+        sl.launches = std::move(bl);
+        sl.ptr_bytes = ptr_bytes;
+        sl.tab_bytes = tab_bytes;
     } else if (dt::log_enabled()) {
-        std::fprintf(stderr, "dt: bucket plan in slot %d reused\n", k);
+        std::fprintf(stderr, "dt: bucket plan in slot %d reused%s\n", k,
+                     capturing ? " under stream capture (slot pinned)" : "");
     }
 
-    const unsigned char *d = static_cast<const unsigned char *>(g->d_plan[k]);
-    const size_t ptr_bytes = g->plan_ptr_bytes[k], tab_bytes = g->plan_tab_bytes[k];
-    const std::vector<dt_group::PlanLaunch> &bl = g->plan_launches[k];
+    dt_group::PlanSlot &sl = g->plans[k];
+    if (capturing) sl.pinned = true;   // a graph now holds this plan's address
+    const unsigned char *d = static_cast<const unsigned char *>(sl.d);
+    const size_t ptr_bytes = sl.ptr_bytes, tab_bytes = sl.tab_bytes;
+    const std::vector<dt_group::PlanLaunch> &bl = sl.launches;
     dt::BucketParams bp;
     bp.ptrs = reinterpret_cast<void *const *>(d);
     bp.P = P;
@@ -986,8 +1015,8 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
             if (st != DT_OK) return st;
         }
     }
-    cudaError_t e2 = cudaEventRecord(g->plan_done[k], s);
-    g->plan_used[k] = true;
+    cudaError_t e2 = capturing ? cudaSuccess : cudaEventRecord(sl.done, s);
+    sl.used = true;
     if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(e2);
 }

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <condition_variable>
 #include <cstdint>
+#include <deque>
 #include <mutex>
 #include <vector>
 
@@ -32,26 +33,32 @@ struct dt_group {
     dt::DevError *h_err = nullptr;   // host-mapped mirror (host view)
     dt::DevError *h_err_dev = nullptr;
 
-    // bucket plans: kPlanSlots pinned host buffers and device buffers.  A slot
-    // keeps the arguments its plan was built for (plan_key) and the launches
-    // it describes, so a call with the same gradients, counts, dtype, op and
-    // cap reuses the uploaded plan; a slot is rebuilt only after its event
-    // says the last kernel reading it ended.
+    // bucket plans: pinned host buffers and device buffers.  A slot keeps the
+    // arguments its plan was built for (key) and the launches it describes,
+    // so a call with the same gradients, counts, dtype, op and cap reuses the
+    // uploaded plan; a slot is rebuilt only after its event says the last
+    // kernel reading it ended.  A slot used by a call under stream capture is
+    // pinned: a CUDA graph holds its device address, so it is never rebuilt,
+    // and new slots are added when every slot is pinned.
     struct PlanLaunch {
         size_t tb, te, start_off;
         uint64_t total, per_block;
         uint32_t blocks;
     };
-    static constexpr int kPlanSlots = 2;
-    void *h_plan[kPlanSlots] = {nullptr, nullptr};
-    void *d_plan[kPlanSlots] = {nullptr, nullptr};
-    size_t plan_bytes[kPlanSlots] = {0, 0};
-    cudaEvent_t plan_done[kPlanSlots] = {nullptr, nullptr};
-    bool plan_used[kPlanSlots] = {false, false};
-    std::vector<uint64_t> plan_key[kPlanSlots];
-    std::vector<PlanLaunch> plan_launches[kPlanSlots];
-    size_t plan_ptr_bytes[kPlanSlots] = {0, 0};
-    size_t plan_tab_bytes[kPlanSlots] = {0, 0};
+    struct PlanSlot {
+        void *h = nullptr;
+        void *d = nullptr;
+        size_t bytes = 0;
+        cudaEvent_t done = nullptr;
+        bool used = false;
+        bool pinned = false;
+        std::vector<uint64_t> key;
+        std::vector<PlanLaunch> launches;
+        size_t ptr_bytes = 0;
+        size_t tab_bytes = 0;
+    };
+    static constexpr int kPlanSlots = 2;   // slots made at create
+    std::deque<PlanSlot> plans;            // stable addresses as it grows
     int next_plan = 0;
 
     // rank-local calls: one host thread per rank meets the others here, like

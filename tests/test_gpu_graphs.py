@@ -104,3 +104,65 @@ def test_bucket_allreduce_graph_replays_its_cached_plan(dt):
         assert dt.dt_group_check(g) == dt.DT_OK
         _, nb = oracle.bucket_plan(counts, 2, cap)
         assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, 4 * (nb - 1)))
+
+
+def test_captured_bucket_plan_survives_other_plans(dt):
+    # A graph holds the device address of the plan it was captured with, so
+    # that plan's slot is pinned: later bucket calls with other arguments use
+    # other slots (new ones when needed) and the graph still replays correctly.
+    P, cap = 2, 32 << 10
+    gen = torch.Generator(device="cuda").manual_seed(13)
+
+    def make(counts):
+        return [[torch.empty(c, dtype=torch.float32, device="cuda") for _ in range(P)] for c in counts]
+
+    def refill(grads):
+        for row in grads:
+            for t in row:
+                t.copy_(torch.randn(t.numel(), generator=gen, device="cuda"))
+
+    A, B, C = make([5000, 17, 9000]), make([300, 12000]), make([64, 64, 64, 70000])
+    s = torch.cuda.Stream()
+    with group(P) as g:
+        with torch.cuda.stream(s):
+            dt.dt_bucket_allreduce(g, A, [5000, 17, 9000], "f32", "sum", cap, s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            dt.dt_bucket_allreduce(g, A, [5000, 17, 9000], "f32", "sum", cap, s)
+        for grads, counts in ((B, [300, 12000]), (C, [64, 64, 64, 70000]), (B, [300, 12000])):
+            with torch.cuda.stream(s):
+                refill(grads)
+                dt.dt_bucket_allreduce(g, grads, counts, "f32", "sum", cap, s)
+            torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            refill(A)
+        torch.cuda.synchronize()
+        ref = [[host(t).copy() for t in row] for row in A]
+        with torch.cuda.stream(s):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    oracle.bucket_allreduce("f32", "sum", ref)
+    for t in range(3):
+        for p in range(P):
+            assert_same(host(A[t][p]), ref[t][p], f"tensor {t} rank {p}")
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")   # the refused call captured nothing
+def test_bucket_capture_without_a_cached_plan_is_refused(dt):
+    P = 2
+    grads = [[torch.ones(1000, device="cuda") for _ in range(P)]]
+    s = torch.cuda.Stream()
+    with group(P) as g:
+        graph = torch.cuda.CUDAGraph()
+        with pytest.raises(dt.DtError) as e:
+            with torch.cuda.graph(graph, stream=s):
+                dt.dt_bucket_allreduce(g, grads, [1000], "f32", "sum", 0, s)
+        assert e.value.status == dt.DT_ERR_UNSUPPORTED
+        torch.cuda.synchronize()
+        # the group and the context are still usable
+        dt.dt_bucket_allreduce(g, grads, [1000], "f32", "sum")
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+        assert float(grads[0][1][999]) == 2.0
