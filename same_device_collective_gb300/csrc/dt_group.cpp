@@ -504,7 +504,11 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
         e = cudaEventCreateWithFlags(&g->rv_ready[r], cudaEventDisableTiming);
     for (int k = 0; k < 2 && e == cudaSuccess; ++k)
         e = cudaEventCreateWithFlags(&g->rv_done[k], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g->comm, cudaStreamNonBlocking);
+    // the async scopes' stream runs at the device's highest priority, so its
+    // blocks take SMs ahead of queued compute blocks as they free up
+    int prio_least = 0, prio_greatest = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&g->comm, cudaStreamNonBlocking, prio_greatest);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->scope_start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
