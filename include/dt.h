@@ -40,8 +40,10 @@
  *             stream order, or the caller makes `stream` wait on an event.
  *   Buffers   Device pointers.  The caller owns them and keeps them alive
  *             until `stream` has passed the call (§五.5 of the same page).
- *             The group owns only its signal window, error word and plan
- *             scratch, allocated once by dt_group_create.
+ *             The group owns only its signal window, error word and bucket
+ *             plan scratch.  dt_group_create allocates them; the plan scratch
+ *             grows only when a bucket plan outgrows it or when every plan
+ *             slot is pinned by a CUDA graph (see "CUDA graphs" below).
  *   Alignment Any alignment is accepted.  When every pointer and size is a
  *             multiple of 16 bytes the kernels move 16-byte vectors; otherwise
  *             they fall back to element-wise access with identical results.
@@ -104,7 +106,8 @@ typedef enum { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2, DT_MIN = 3, DT_SUM_STEPWISE =
 
 /* Create a group of world_size (1..DT_MAX_RANKS) logical ranks on CUDA device
  * cuda_device.  Allocates the P x P int32 signal window, the error word and
- * the plan scratch on that device, so every later call is allocation-free.
+ * two 1 MiB bucket-plan slots on that device; later calls allocate nothing
+ * except a bucket all-reduce whose plan needs a larger or an extra slot.
  * The device-side wait limit is read from the environment variable
  * DT_TIMEOUT_MS (default 2000).  Like the TensorStore constructor, which
  * starts all participants from one state, the window starts at zero.
@@ -252,11 +255,12 @@ dt_status dt_bucket_plan(const size_t *counts, size_t n_tensors, size_t elem_byt
 /* Signal-window barrier: "Barrier：仅信号（Signals Only）".  The group keeps
  * an int32 window win[P][P] in HBM (row r of rank q's window is win[q][r]).
  * The g-th barrier (1-based generation, bumped by every call) is one kernel
- * in which each rank is one warp: rank r adds 1 (AtomicAdd, release) to
- * win[q][r] of every peer q != r, then waits until win[r][s] >= g (Ge,
- * acquire) for every s != r.  Afterwards win[r][s] == g for s != r and
- * win[r][r] == 0.  Each wait gives up after the group's time limit and
- * records DT_ERR_TIMEOUT. */
+ * in which each rank is one warp: rank r adds 1 (AtomicAdd) to win[q][r] of
+ * every peer q != r, then waits until win[r][s] >= g (Ge) for every s != r.
+ * Afterwards win[r][s] == g for s != r and win[r][r] == 0.  Stream order
+ * orders the data around the barrier kernel, so its adds and polls are
+ * relaxed GPU-scope atomics and loads.  Each wait gives up after the group's
+ * time limit and records DT_ERR_TIMEOUT. */
 dt_status dt_barrier(dt_group_t g, int rank, void *stream);
 
 /* Allocation-free fused bucket all-reduce.  The pages have no counterpart:
@@ -272,9 +276,10 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
  * this library (every GPU that loads the library holds it until the process
  * exits) and are staged from a fixed host array: the call allocates nothing.
  * Tables that do not fit (n_tensors * (P * 8 + 24) bytes plus 4 bytes per
- * thread block of every bucket, at most a few hundred blocks per bucket) or
- * more than 4096 buckets return DT_ERR_TOO_LARGE before anything is
- * enqueued.  Every call shares the array and leaves its contents behind;
+ * thread block of every bucket: one block per 2048 bf16 or 1024 fp32
+ * elements, at most 16 per resident block slot, so about 40 full 25 MiB
+ * buckets) or more than 4096 buckets return DT_ERR_TOO_LARGE before anything
+ * is enqueued.  Every call shares the array and leaves its contents behind;
  * calls that overlap on the GPU (unordered streams) race on it, calls on one
  * stream do not.  No signal barrier runs between buckets (there is no group
  * window); stream order orders them.  The first call on each device looks up
