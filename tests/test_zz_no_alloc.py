@@ -85,3 +85,26 @@ def test_static_bucket_allreduce_rejects_tables_past_the_fixed_array(dt):
     assert dt.dt_launch_count() == n0
     torch.cuda.synchronize()
     assert torch.count_nonzero(buf).item() == 0
+
+
+def test_static_bucket_allreduce_full_workload(dt):
+    # The 200-gradient, 8-rank bf16 workload (7 buckets of up to 25 MiB): its
+    # tables (about 200 KB with one-pass bucket slices) fit the fixed array,
+    # and the result equals the group-based call's, bit for bit.
+    from same_device_collective_gb300 import workloads as wl
+    w = wl.bucket_grads(device="cuda")
+    counts = w.meta["counts"]
+    a = w.inputs
+    b = [[x.clone() for x in row] for row in a]
+    torch.cuda.synchronize()
+    dt.dt_bucket_allreduce_static(8, a, counts, "bf16", "avg", bucket_cap_bytes=wl.BUCKET_CAP_BYTES)
+    g = dt.dt_group_create(8, torch.cuda.current_device())
+    try:
+        dt.dt_bucket_allreduce(g, b, counts, "bf16", "avg", bucket_cap_bytes=wl.BUCKET_CAP_BYTES)
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    finally:
+        dt.dt_group_destroy(g)
+    for t in range(len(counts)):
+        for p in range(8):
+            assert torch.equal(a[t][p], b[t][p]), f"tensor {t} rank {p}"
