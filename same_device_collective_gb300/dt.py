@@ -111,8 +111,15 @@ def _ptr(x) -> int:
     return x.data_ptr()
 
 
+_VP_ARRAY_TYPES: dict = {}
+
+
 def _ptr_array(xs: Sequence) -> ctypes.Array:
-    return (ctypes.c_void_p * max(len(xs), 1))(*[_ptr(x) for x in xs])
+    n = len(xs) or 1
+    t = _VP_ARRAY_TYPES.get(n)
+    if t is None:                        # building an array type costs more than filling it
+        t = _VP_ARRAY_TYPES[n] = ctypes.c_void_p * n
+    return t(*[_ptr(x) for x in xs])
 
 
 def pointer_table(rows: Sequence[Sequence]) -> np.ndarray:
