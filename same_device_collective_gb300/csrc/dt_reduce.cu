@@ -23,17 +23,22 @@
 namespace dt {
 namespace {
 
+// Vector positions per thread per iteration (U), measured on GB300: a
+// ReduceScatter keeps 8 loads of 16 bytes in flight per thread (U = 8 / P,
+// 16 loads at P > 8), which its step needs; an AllReduce does best with one
+// position per thread at every size (a P=2 fp32 AllReduce of 4 MiB per rank
+// 3.8 -> 2.55 us in a CUDA graph, 16 MiB per rank +11%, P=4 256 MiB +3%),
+// because its P output stores per position already keep the thread busy.
 template <int PMAX>
-struct Unroll {   // 8 loads of 16 bytes in flight per thread (16 at P > 8)
-    static constexpr int U = PMAX >= 8 ? 1 : 8 / PMAX;
+struct Unroll {
+    static constexpr int kScatter = PMAX >= 8 ? 1 : 8 / PMAX;
 };
 
-template <int DT, int OP, int PMAX>
+template <int DT, int OP, int PMAX, int U>
 __global__ void __launch_bounds__(kThreads)
 reduce_vec_kernel(const __grid_constant__ ReduceParams p)
 {
     pdl_begin();
-    constexpr int U = Unroll<PMAX>::U;
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     const int P = p.P;
     const int j = blockIdx.y;
@@ -94,32 +99,38 @@ struct KernelInfo {
     int per_vec_iter = 1;   // vectors (or elements) per thread per iteration
 };
 
-template <int DT, int OP>
-KernelInfo pick_vec(int P)
+template <int DT, int OP, int PMAX>
+KernelInfo pick_unroll(bool scatter)
 {
-    KernelInfo k;
-    if (P <= 2) { k.fn = reduce_vec_kernel<DT, OP, 2>; k.per_vec_iter = Unroll<2>::U; }
-    else if (P <= 4) { k.fn = reduce_vec_kernel<DT, OP, 4>; k.per_vec_iter = Unroll<4>::U; }
-    else if (P <= 8) { k.fn = reduce_vec_kernel<DT, OP, 8>; k.per_vec_iter = Unroll<8>::U; }
-    else { k.fn = reduce_vec_kernel<DT, OP, 16>; k.per_vec_iter = Unroll<16>::U; }
-    return k;
+    constexpr int U = Unroll<PMAX>::kScatter;
+    if (scatter && U > 1) return KernelInfo{reduce_vec_kernel<DT, OP, PMAX, U>, U};
+    return KernelInfo{reduce_vec_kernel<DT, OP, PMAX, 1>, 1};
+}
+
+template <int DT, int OP>
+KernelInfo pick_vec(int P, bool scatter)
+{
+    if (P <= 2) return pick_unroll<DT, OP, 2>(scatter);
+    if (P <= 4) return pick_unroll<DT, OP, 4>(scatter);
+    if (P <= 8) return pick_unroll<DT, OP, 8>(scatter);
+    return pick_unroll<DT, OP, 16>(scatter);
 }
 
 template <int DT>
-KernelInfo pick_op(int op, int P, bool vec)
+KernelInfo pick_op(int op, int P, bool vec, bool scatter)
 {
     KernelInfo k;
     switch (op) {
-    case DT_SUM: k = vec ? pick_vec<DT, DT_SUM>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_SUM>, 1}; break;
-    case DT_MAX: k = vec ? pick_vec<DT, DT_MAX>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_MAX>, 1}; break;
-    case DT_MIN: k = vec ? pick_vec<DT, DT_MIN>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_MIN>, 1}; break;
+    case DT_SUM: k = vec ? pick_vec<DT, DT_SUM>(P, scatter) : KernelInfo{reduce_scalar_kernel<DT, DT_SUM>, 1}; break;
+    case DT_MAX: k = vec ? pick_vec<DT, DT_MAX>(P, scatter) : KernelInfo{reduce_scalar_kernel<DT, DT_MAX>, 1}; break;
+    case DT_MIN: k = vec ? pick_vec<DT, DT_MIN>(P, scatter) : KernelInfo{reduce_scalar_kernel<DT, DT_MIN>, 1}; break;
     case DT_AVG:
         if constexpr (DT != DT_I32)
-            k = vec ? pick_vec<DT, DT_AVG>(P) : KernelInfo{reduce_scalar_kernel<DT, DT_AVG>, 1};
+            k = vec ? pick_vec<DT, DT_AVG>(P, scatter) : KernelInfo{reduce_scalar_kernel<DT, DT_AVG>, 1};
         break;
     case DT_SUM_STEPWISE:   // only bf16 rounds between adds; the launcher maps the rest to SUM
         if constexpr (DT == DT_BF16)
-            k = vec ? pick_vec<DT, DT_SUM_STEPWISE>(P)
+            k = vec ? pick_vec<DT, DT_SUM_STEPWISE>(P, scatter)
                     : KernelInfo{reduce_scalar_kernel<DT, DT_SUM_STEPWISE>, 1};
         break;
     default: break;
@@ -136,9 +147,10 @@ cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bo
 {
     KernelInfo k;
     if (op == DT_SUM_STEPWISE && dtype != DT_BF16) op = DT_SUM;   // identical results
-    if (dtype == DT_F32) k = pick_op<DT_F32>(op, p.P, vec);
-    else if (dtype == DT_BF16) k = pick_op<DT_BF16>(op, p.P, vec);
-    else if (dtype == DT_I32) k = pick_op<DT_I32>(op, p.P, vec);
+    const bool scatter = jobs > 1;
+    if (dtype == DT_F32) k = pick_op<DT_F32>(op, p.P, vec, scatter);
+    else if (dtype == DT_BF16) k = pick_op<DT_BF16>(op, p.P, vec, scatter);
+    else if (dtype == DT_I32) k = pick_op<DT_I32>(op, p.P, vec, scatter);
     if (!k.fn) return cudaErrorInvalidValue;
 
     int resident = 0;
