@@ -52,6 +52,27 @@ __device__ __forceinline__ bool take_f(float x, float best)
     return (x != x) || (OP == DT_MAX ? x > best : x < best);
 }
 
+// MAX / MIN on two packed bf16 elements: per 16-bit half, x replaces the
+// running choice where x is a NaN or compares strictly above (MAX) / below
+// (MIN) it.  The bf16x2 comparisons give an all-ones half where they hold;
+// ordered comparisons are false against a NaN and between equal values (+0
+// and -0 included), so ties keep the lower rank's element and a NaN, once
+// chosen, gives way only to a later NaN.  The halves move as raw bits, so the
+// chosen element (NaN payload included) is stored unchanged: the same choice
+// as take_f on the widened values, since bf16 -> fp32 is exact.
+template <int OP>
+__device__ __forceinline__ uint32_t select_bf16x2(uint32_t x, uint32_t best)
+{
+    uint32_t beats, nan;
+    if constexpr (OP == DT_MAX)
+        asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(beats) : "r"(x), "r"(best));
+    else
+        asm("set.lt.u32.bf16x2 %0, %1, %2;" : "=r"(beats) : "r"(x), "r"(best));
+    asm("set.nan.u32.bf16x2 %0, %1, %1;" : "=r"(nan) : "r"(x));
+    const uint32_t m = beats | nan;
+    return (x & m) | (best & ~m);
+}
+
 // fp32 -> bf16 (round to nearest even) -> fp32: where a stepwise sum lands.
 __device__ __forceinline__ float round_bf16(float f)
 {
@@ -123,19 +144,12 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
                 }
                 o[k] = pack_bf16x2(lo, hi);
             } else {
-                // the running choice is kept as the widened fp32 value; a select
-                // moves bits unchanged, so the chosen bf16 element (NaN payload
-                // included) is recovered from those bits by a shift
-                float flo = bf16_lo(w[0][k]), fhi = bf16_hi(w[0][k]);
+                // both elements of the word at once, without widening
+                uint32_t best = w[0][k];
 #pragma unroll
-                for (int r = 1; r < PMAX; ++r) {
-                    if (r < P) {
-                        const float xl = bf16_lo(w[r][k]), xh = bf16_hi(w[r][k]);
-                        flo = take_f<OP>(xl, flo) ? xl : flo;
-                        fhi = take_f<OP>(xh, fhi) ? xh : fhi;
-                    }
-                }
-                o[k] = (__float_as_uint(flo) >> 16) | (__float_as_uint(fhi) & 0xFFFF0000u);
+                for (int r = 1; r < PMAX; ++r)
+                    if (r < P) best = select_bf16x2<OP>(w[r][k], best);
+                o[k] = best;
             }
         }
     }

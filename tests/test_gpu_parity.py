@@ -114,6 +114,55 @@ def test_allreduce_nan_and_signed_zero(dt):
     assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
 
 
+def _special_bits(dtype: str, P: int, n: int, seed: int) -> list:
+    """Rank inputs drawn from the values MAX/MIN must treat with care: NaNs
+    with distinct payloads (quiet and signalling, both signs), +0 and -0,
+    subnormals of both signs, infinities, and a few normal values, so that
+    ties, NaN runs and subnormal orderings occur at every rank position."""
+    rng = np.random.default_rng(seed)
+    if dtype == "bf16":
+        pool = np.array([0x0000, 0x8000, 0x0001, 0x0002, 0x007F, 0x8001, 0x807F,
+                         0x7F80, 0xFF80, 0x7FC0, 0x7FC1, 0xFFC3, 0x7F81, 0xFF85,
+                         0x3F80, 0xBF80, 0x4000, 0x0080, 0x8080], np.uint16)
+    else:
+        pool = np.array([0x00000000, 0x80000000, 0x00000001, 0x00000002, 0x007FFFFF,
+                         0x80000001, 0x807FFFFF, 0x7F800000, 0xFF800000, 0x7FC00000,
+                         0x7FC00001, 0xFFC00003, 0x7F800001, 0xFF800005, 0x3F800000,
+                         0xBF800000, 0x40000000, 0x00800000, 0x80800000], np.uint32)
+    return [pool[rng.integers(0, pool.size, n)] for _ in range(P)]
+
+
+def _device_from_bits(bits: np.ndarray, dtype: str) -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(bits.view(np.float32).copy()).cuda()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("op", ["max", "min"])
+@pytest.mark.parametrize("P", [2, 3, 8, 16])
+def test_max_min_special_values_bit_exact(dt, dtype, op, P):
+    # every bit compared, NaN payloads included: the result is the chosen
+    # rank's element, unchanged (AllReduce, then ReduceScatter of P shards)
+    m = 4099                                   # vector positions plus a ragged tail
+    bits = _special_bits(dtype, P, P * m, 40 + P)
+    xs = [_device_from_bits(b, dtype) for b in bits]
+    n = P * m
+    outs = [torch.empty_like(x) for x in xs]
+    shards = [torch.empty(m, dtype=TORCH_DTYPE[dtype], device="cuda") for _ in range(P)]
+    with group(P) as g:
+        dt.dt_allreduce(g, dt.DT_ALL_RANKS, xs, outs, n, dtype, op)
+        dt.dt_reduce_scatter(g, dt.DT_ALL_RANKS, xs, shards, m, dtype, op)
+        torch.cuda.synchronize()
+    view = np.uint16 if dtype == "bf16" else np.float32
+    want = oracle.allreduce(dtype, op, [b.view(view).copy() for b in bits])
+    for q in range(P):
+        assert_same(host(outs[q]), want[q], f"allreduce rank {q}")
+    want = oracle.reduce_scatter(dtype, op, [b.view(view).copy() for b in bits])
+    for r in range(P):
+        assert_same(host(shards[r]), want[r], f"reduce_scatter rank {r}")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "i32"])
 @pytest.mark.parametrize("P", [2, 3, 8, 16])
 def test_sum_stepwise_matches_oracle(dt, dtype, P):

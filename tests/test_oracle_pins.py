@@ -292,6 +292,38 @@ def test_max_min_nan_and_signed_zero_hand_cases():
     assert bits32(oracle.reduce("f32", "min", [f32([0.0]), f32([-0.0])]))[0] == 0x00000000
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_max_min_special_values_closed_form(dtype, op):
+    # Inputs from NaNs with distinct payloads, +-0, subnormals, infinities and
+    # normals.  Closed form of the selection rule, element by element: if any
+    # rank holds a NaN, the result is the highest such rank's element, bits
+    # unchanged; otherwise it is the element of the lowest rank whose value
+    # equals numpy's max (min) of the widened values.
+    if dtype == "bf16":
+        pool = np.array([0x0000, 0x8000, 0x0001, 0x007F, 0x8001, 0x807F, 0x7F80, 0xFF80,
+                         0x7FC0, 0x7FC1, 0xFFC3, 0x7F81, 0x3F80, 0xBF80, 0x0080], np.uint16)
+        widen = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        pool = np.array([0x00000000, 0x80000000, 0x00000001, 0x007FFFFF, 0x80000001,
+                         0x7F800000, 0xFF800000, 0x7FC00000, 0x7FC00001, 0xFFC00003,
+                         0x7F800001, 0x3F800000, 0xBF800000, 0x00800000], np.uint32)
+        widen = lambda b: b.view(np.float32).astype(np.float64)
+    P, n = 6, 4000
+    r = np.random.default_rng(7)
+    bits = np.stack([pool[r.integers(0, pool.size, n)] for _ in range(P)])
+    vals = widen(bits.reshape(-1)).reshape(P, n)
+    ins = [bits[p].view(np.uint16 if dtype == "bf16" else np.float32).copy() for p in range(P)]
+    got = oracle.reduce(dtype, op, ins).view(bits.dtype)
+    isnan = np.isnan(vals)
+    last_nan = P - 1 - np.argmax(isnan[::-1], axis=0)
+    clean = np.where(isnan, -np.inf if op == "max" else np.inf, vals)
+    best = clean.max(0) if op == "max" else clean.min(0)
+    first_best = np.argmax(clean == best, axis=0)
+    pick = np.where(isnan.any(0), last_nan, first_best)
+    assert np.array_equal(got, bits[pick, np.arange(n)])
+
+
 def test_int32_sum_wraps_and_max_min_equal_numpy():
     big = np.array([2 ** 31 - 1], dtype=np.int32)
     one = np.array([1], dtype=np.int32)
