@@ -46,8 +46,18 @@ __device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
 constexpr int kBulkThreads = 32;
 
 // Tile size and pipeline depth, measured on GB300 per launch layout:
-//   kStream: the P^2 single-destination segments of an AllToAll stream best
-//            as 16 KiB tiles 12 deep;
+//   kStream: the P^2 single-destination segments of an AllToAll of up to 8
+//            ranks whose data does not fit in L2 stream best as 16 KiB tiles
+//            12 deep, one block per SM (8 ranks, 64-512 MiB per rank:
+//            7.0-7.1 TB/s; every shallower or split shape tried measured
+//            6.4-6.6);
+//   kSplit:  the other AllToAlls of 8 or more ranks: 16 KiB tiles 4 deep, so
+//            three blocks share an SM and three threads issue its copies.
+//            A block's single issuing thread bounds the 12-deep shape when
+//            the copies come from L2 (8 ranks, 4 MiB per rank: 5.5 -> 9.1
+//            TB/s) and when the 256-entry segment table of 16 ranks makes
+//            each tile's segment lookup slow (16 ranks, 4-256 MiB per rank:
+//            4.7-5.9 -> 6.3-7.7 TB/s);
 //   kGather: few segments (equal or uneven shards, shared or per-rank
 //            outputs of moderate size, row-block copies): 32 KiB x 6;
 //   kWide:   large launches whose segments each store to 2..8 destinations
@@ -56,7 +66,7 @@ constexpr int kBulkThreads = 32;
 //            smaller ones (the RS+AG step 105.1 -> 104.2 us).
 // Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
 // bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
-enum BulkKind { kStream = 0, kGather = 1, kWide = 2 };
+enum BulkKind { kStream = 0, kGather = 1, kWide = 2, kSplit = 3 };
 
 // Blocks per launch.  One block per SM holds a shape's stages; extra blocks
 // run in later waves, and the hardware hands each to whichever SM frees up
@@ -70,15 +80,15 @@ template <int KIND>
 uint64_t bulk_grid(uint64_t tiles, int resident)
 {
     const bool plenty = tiles >= 16 * (uint64_t)resident;
-    const uint64_t waves = KIND == kStream ? 1 : plenty ? 8 : KIND == kWide ? 4 : 1;
+    const uint64_t waves = KIND == kStream || KIND == kSplit ? 1 : plenty ? 8 : KIND == kWide ? 4 : 1;
     const uint64_t cap = (uint64_t)resident * waves;
     return tiles < cap ? tiles : cap;
 }
 
 template <int KIND>
 struct BulkShape {
-    static constexpr int kStages = KIND == kStream ? 12 : KIND == kGather ? 6 : 2;
-    static constexpr int kTile = KIND == kStream ? 16384 : KIND == kGather ? 32768 : 98304;
+    static constexpr int kStages = KIND == kStream ? 12 : KIND == kSplit ? 4 : KIND == kGather ? 6 : 2;
+    static constexpr int kTile = KIND == kStream || KIND == kSplit ? 16384 : KIND == kGather ? 32768 : 98304;
     static constexpr size_t kBarBytes = ((size_t)kStages * 8 + 127) / 128 * 128;
     static constexpr size_t kSmem = kBarBytes + (size_t)kStages * kTile;
     static_assert(kBarBytes >= (size_t)kStages * 8, "mbarrier area too small");
@@ -293,8 +303,13 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
         cut_tiles(p, BulkShape<kWide>::kTile) >= 4 * (uint64_t)sm_count(device))
         return launch_bulk<NSEG, NOUT, kWide>(p, device, s);
     if (NSEG > DT_MAX_RANKS) {
-        cut_tiles(p, BulkShape<kStream>::kTile);
-        return launch_bulk<NSEG, NOUT, kStream>(p, device, s);
+        const uint64_t tiles = cut_tiles(p, BulkShape<kStream>::kTile);
+        // with a tile or less per SM, one block per SM spreads the copies
+        // over every SM's copy engine (8 ranks, 256 KiB per rank: the split
+        // shape lost 16%)
+        if ((p.nseg <= 64 && 2 * src_bytes > l2_bytes(device)) || tiles <= (uint64_t)sm_count(device))
+            return launch_bulk<NSEG, NOUT, kStream>(p, device, s);
+        return launch_bulk<NSEG, NOUT, kSplit>(p, device, s);
     }
     cut_tiles(p, BulkShape<kGather>::kTile);
     return launch_bulk<NSEG, NOUT, kGather>(p, device, s);

@@ -99,6 +99,19 @@ int sm_count(int device)
     return n;
 }
 
+uint64_t l2_bytes(int device)
+{
+    static std::mutex mu;
+    static std::unordered_map<int, uint64_t> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(device);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, device) != cudaSuccess || n < 0) n = 0;
+    cache[device] = (uint64_t)n;
+    return (uint64_t)n;
+}
+
 cudaError_t resident_blocks(const void *fn, int threads, int device, int *out, size_t dyn_smem)
 {
     static std::mutex mu;

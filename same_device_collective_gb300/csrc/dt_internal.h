@@ -189,6 +189,8 @@ cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t s
     return e;
 }
 int sm_count(int device);
+// Bytes of L2 cache on the device (cached per device).
+uint64_t l2_bytes(int device);
 // SMs x blocks of `fn` one SM holds at once (cached per kernel and device).
 cudaError_t resident_blocks(const void *fn, int threads, int device, int *out,
                             size_t dyn_smem = 0);

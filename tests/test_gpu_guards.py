@@ -158,6 +158,28 @@ def test_all_to_all_writes_only_its_outputs(dt, P, chunk_bytes):
         assert_same(host(o.view(torch.uint8)), want[j], f"rank {j}")
 
 
+@pytest.mark.parametrize("P,chunk_bytes", [(16, 7 * 16384 + 48), (8, (2 << 20) + 48)])
+def test_bulk_all_to_all_shapes_write_only_their_outputs(dt, P, chunk_bytes):
+    # The two bulk-copy shapes of an AllToAll of 8+ ranks, each segment ending
+    # in a 48-byte partial tile: 16 ranks of ~1.8 MiB (data fits in L2: four
+    # stages, three blocks per SM) and 8 ranks of ~16 MiB (data larger than
+    # half of L2: twelve stages, one block per SM).
+    gen = torch.Generator(device="cuda").manual_seed(P + chunk_bytes)
+    xs = [torch.randint(0, 256, (P * chunk_bytes,), generator=gen, dtype=torch.uint8, device="cuda")
+          for _ in range(P)]
+    snap = snapshot(xs)
+    want = oracle.all_to_all(snap)
+    outs = [Guarded(P * chunk_bytes) for _ in range(P)]
+    with group(P) as g:
+        dt.dt_all_to_all(g, dt.DT_ALL_RANKS, xs, [o.view(torch.uint8) for o in outs], chunk_bytes)
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    assert unchanged(xs, snap)
+    for j, o in enumerate(outs):
+        assert o.intact(), f"rank {j}"
+        assert_same(host(o.view(torch.uint8)), want[j], f"rank {j}")
+
+
 # ------------------------------------------------------- bucket all-reduce
 @pytest.mark.parametrize("dtype,op", [("bf16", "avg"), ("f32", "sum")])
 @pytest.mark.parametrize("cap", [4096, 25 << 20])
