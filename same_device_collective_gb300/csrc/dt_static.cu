@@ -31,7 +31,14 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)1 << 20;
 constexpr int kMaxDevices = 64;
 
-__device__ __align__(256) unsigned char g_bucket_scratch[kStaticScratchBytes];
+}  // namespace
+
+// The fixed device array: file scope, internal linkage, one copy on every
+// device that loads the library.  In host code its name is only a host-side
+// stand-in; scratch_address() looks up the device address.
+static __device__ __align__(256) unsigned char g_bucket_scratch[kStaticScratchBytes];
+
+namespace {
 
 // Host staging of the same size: copied with a pageable cudaMemcpyAsync,
 // which returns once the bytes have left this array.
