@@ -106,6 +106,35 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
                 if (r < P) acc = pick_i<OP>(acc, (int32_t)w[r][k]);
             o[k] = (uint32_t)acc;
         }
+    } else if constexpr (DT == DT_F32 && (OP == DT_MAX || OP == DT_MIN) && PMAX == 16) {
+        // More than 8 ranks: ranks 0..7 and 8..P-1 are scanned as two
+        // independent chains, then the upper chain's choice replaces the lower
+        // one's by the same rule.  Splitting the scan cannot change the
+        // choice: either way it is the last NaN if there is one, else the
+        // first element equal to the extreme value.
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float lo = __uint_as_float(w[0][k]);
+#pragma unroll
+            for (int r = 1; r < 8; ++r) {
+                if (r < P) {
+                    const float x = __uint_as_float(w[r][k]);
+                    lo = take_f<OP>(x, lo) ? x : lo;
+                }
+            }
+            if (P > 8) {
+                float hi = __uint_as_float(w[8][k]);
+#pragma unroll
+                for (int r = 9; r < 16; ++r) {
+                    if (r < P) {
+                        const float x = __uint_as_float(w[r][k]);
+                        hi = take_f<OP>(x, hi) ? x : hi;
+                    }
+                }
+                lo = take_f<OP>(hi, lo) ? hi : lo;
+            }
+            o[k] = __float_as_uint(lo);
+        }
     } else if constexpr (DT == DT_F32) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {

@@ -140,7 +140,7 @@ def _device_from_bits(bits: np.ndarray, dtype: str) -> torch.Tensor:
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("op", ["max", "min"])
-@pytest.mark.parametrize("P", [2, 3, 8, 16])
+@pytest.mark.parametrize("P", [2, 3, 8, 12, 16])
 def test_max_min_special_values_bit_exact(dt, dtype, op, P):
     # every bit compared, NaN payloads included: the result is the chosen
     # rank's element, unchanged (AllReduce, then ReduceScatter of P shards)
