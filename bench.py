@@ -745,6 +745,7 @@ NCU_CASES = {
     "allreduce_small": ("reduce_vec_kernel", 2, "AllReduce kSum f32, P=2, 2^20 per rank"),
     "bucket": ("bucket_kernel", 14, "bucket AllReduce kAvg bf16, P=8, 200 tensors, 25 MiB buckets"),
     "all_to_all": ("copy_bulk_kernel", 2, "AllToAll bf16, P=8, [8192, 4096] per rank"),
+    "all_to_all_p16": ("copy_bulk_kernel", 2, "AllToAll bf16, P=16, [8192, 2048] per rank"),
     "uneven_all_gather": ("copy_bulk_kernel", 2,
                           "uneven AllGather int32, P=8, rows U[1, 2048] x 4096, per-rank outputs"),
     "barrier": ("barrier_kernel", 2, "signal-window barrier, P=16"),
@@ -777,6 +778,12 @@ def run_ncu_case(name):
         nbytes = w.inputs[0].numel() * 2
         g = dt.dt_group_create(8, dev.index)
         call = lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes // 8)
+    elif name == "all_to_all_p16":
+        w = workloads.all_to_all_tokens(P=16, rows=8192, cols=2048, device=str(dev))
+        outs = [torch.empty_like(x) for x in w.inputs]
+        nbytes = w.inputs[0].numel() * 2
+        g = dt.dt_group_create(16, dev.index)
+        call = lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes // 16)
     elif name == "uneven_all_gather":
         w = workloads.uneven_gather(max_rows=2048, device=str(dev))
         rws = w.meta["rows"]
