@@ -302,7 +302,7 @@ def test_reduce_scatter_then_all_gather_equals_allreduce(dt, dtype, op):
 # ------------------------------------------------------------ bucket + barrier
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("op", ["avg", "sum"])
-@pytest.mark.parametrize("P", [2, 3, 8])
+@pytest.mark.parametrize("P", [1, 2, 3, 8, 16])
 def test_bucket_allreduce_matches_oracle(dt, dtype, op, P):
     rng = np.random.default_rng(P + 31)
     counts = [0, 1, 7, 1000, 40_000, 70_001, 5, 32_768, 3]
