@@ -63,10 +63,15 @@ constexpr int kBulkThreads = 32;
 //   kWide:   large launches whose segments each store to 2..8 destinations
 //            (per-rank gathers): every tile is stored several times, so each
 //            stage stays busy long enough that two 96 KiB stages beat more,
-//            smaller ones (the RS+AG step 105.1 -> 104.2 us).
+//            smaller ones when tiles are plentiful (16+ per SM);
+//   kWideSplit: the same gathers with 4-16 of those tiles per SM: 32 KiB x 3,
+//            two blocks per SM, so two threads per SM issue the stores (the
+//            4-rank gather of 16 MiB shards in the RS+AG step 51.0 -> 47.4 us
+//            with events around it, the step 98.4 -> 95.8 us; 2 ranks of
+//            64 MiB +2%).
 // Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
 // bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
-enum BulkKind { kStream = 0, kGather = 1, kWide = 2, kSplit = 3 };
+enum BulkKind { kStream = 0, kGather = 1, kWide = 2, kSplit = 3, kWideSplit = 4 };
 
 // Blocks per launch.  One block per SM holds a shape's stages; extra blocks
 // run in later waves, and the hardware hands each to whichever SM frees up
@@ -80,15 +85,18 @@ template <int KIND>
 uint64_t bulk_grid(uint64_t tiles, int resident)
 {
     const bool plenty = tiles >= 16 * (uint64_t)resident;
-    const uint64_t waves = KIND == kStream || KIND == kSplit ? 1 : plenty ? 8 : KIND == kWide ? 4 : 1;
+    const uint64_t waves = KIND == kStream || KIND == kSplit ? 1
+                           : plenty ? 8 : KIND == kWide || KIND == kWideSplit ? 4 : 1;
     const uint64_t cap = (uint64_t)resident * waves;
     return tiles < cap ? tiles : cap;
 }
 
 template <int KIND>
 struct BulkShape {
-    static constexpr int kStages = KIND == kStream ? 12 : KIND == kSplit ? 4 : KIND == kGather ? 6 : 2;
-    static constexpr int kTile = KIND == kStream || KIND == kSplit ? 16384 : KIND == kGather ? 32768 : 98304;
+    static constexpr int kStages = KIND == kStream ? 12 : KIND == kSplit ? 4 : KIND == kGather ? 6
+                                   : KIND == kWideSplit ? 3 : 2;
+    static constexpr int kTile = KIND == kStream || KIND == kSplit ? 16384
+                                 : KIND == kGather || KIND == kWideSplit ? 32768 : 98304;
     static constexpr size_t kBarBytes = ((size_t)kStages * 8 + 127) / 128 * 128;
     static constexpr size_t kSmem = kBarBytes + (size_t)kStages * kTile;
     static_assert(kBarBytes >= (size_t)kStages * 8, "mbarrier area too small");
@@ -299,9 +307,17 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
     // least 4 per SM; at 2 per SM a 16 MiB-per-rank P=2 gather lost 17%), and
     // they stop paying at 16 destinations, where each tile carries 1.5 MiB of
     // stores and the last wave runs half empty.
-    if (max_dst > 1 && max_dst <= 8 &&
-        cut_tiles(p, BulkShape<kWide>::kTile) >= 4 * (uint64_t)sm_count(device))
-        return launch_bulk<NSEG, NOUT, kWide>(p, device, s);
+    if (max_dst > 1 && max_dst <= 8) {
+        const uint64_t sms = (uint64_t)sm_count(device);
+        const uint64_t wide = cut_tiles(p, BulkShape<kWide>::kTile);
+        if (wide >= 16 * sms) return launch_bulk<NSEG, NOUT, kWide>(p, device, s);
+        // smaller gathers keep the 32 KiB x 6 shape below (a 2-rank gather of
+        // 16 MiB shards lost 9% on the split shape)
+        if (wide >= 4 * sms) {
+            cut_tiles(p, BulkShape<kWideSplit>::kTile);
+            return launch_bulk<NSEG, NOUT, kWideSplit>(p, device, s);
+        }
+    }
     if (NSEG > DT_MAX_RANKS) {
         const uint64_t tiles = cut_tiles(p, BulkShape<kStream>::kTile);
         // with a tile or less per SM, one block per SM spreads the copies

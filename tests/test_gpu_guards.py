@@ -250,12 +250,15 @@ def test_placement_conversions_write_only_their_outputs(dt):
         assert_same(host(o.view(torch.int32)), want_a2a[j], f"all-to-all rank {j}")
 
 
-@pytest.mark.parametrize("rows,shared", [([8193, 8190], False), ([3073, 3070], True)])
+@pytest.mark.parametrize("rows,shared", [([8193, 8190], False), ([3073, 3070], True),
+                                         ([1025, 1023, 1024, 1021], False)])
 def test_large_gathers_in_waves_write_only_their_outputs(dt, rows, shared):
     # Big enough for the bulk copy's multi-wave grids: per-rank outputs of two
     # ~128 MiB shards take 96 KiB tiles in 8 waves, a shared output of two
-    # ~48 MiB shards 32 KiB tiles in 8 waves; both shards end in a partial tile.
-    P, row_bytes = 2, 16384
+    # ~48 MiB shards 32 KiB tiles in 8 waves, per-rank outputs of four ~16 MiB
+    # shards 32 KiB tiles on two blocks per SM in 4 waves; every shard ends in
+    # a partial tile.
+    P, row_bytes = len(rows), 16384
     gen = torch.Generator(device="cuda").manual_seed(sum(rows))
     xs = [torch.randint(0, 256, (c * row_bytes,), generator=gen, device="cuda", dtype=torch.uint8)
           for c in rows]
