@@ -60,6 +60,13 @@ constexpr int kBulkThreads = 32;
 //            4.7-5.9 -> 6.3-7.7 TB/s);
 //   kGather: few segments (equal or uneven shards, shared or per-rank
 //            outputs of moderate size, row-block copies): 32 KiB x 6;
+//   kGatherSplit: the same launches with at least 3 tiles of 16 KiB per SM
+//            and at most 8 destinations per segment: 16 KiB x 4, three
+//            blocks per SM (2-rank AllToAll of 64 MiB per rank +3%, 16 MiB
+//            +8%; ReplicateToShard of 4 ranks +2%; 2-, 4- and 8-rank gathers
+//            of 1-4 MiB shards +5-8%).  With fewer tiles the blocks crowd onto
+//            fewer SMs (4-rank gather of 1 MiB shards -12%), and 16-rank
+//            gathers, with 16 stores per tile, lost 3-22%;
 //   kWide:   large launches whose segments each store to 2..8 destinations
 //            (per-rank gathers): every tile is stored several times, so each
 //            stage stays busy long enough that two 96 KiB stages beat more,
@@ -71,7 +78,7 @@ constexpr int kBulkThreads = 32;
 //            64 MiB +2%).
 // Shared memory: the stages' mbarriers (8 bytes each, area rounded up to 128
 // bytes so the tile buffers stay 128-byte aligned), then the tile buffers.
-enum BulkKind { kStream = 0, kGather = 1, kWide = 2, kSplit = 3, kWideSplit = 4 };
+enum BulkKind { kStream = 0, kGather = 1, kWide = 2, kSplit = 3, kWideSplit = 4, kGatherSplit = 5 };
 
 // Blocks per launch.  One block per SM holds a shape's stages; extra blocks
 // run in later waves, and the hardware hands each to whichever SM frees up
@@ -93,9 +100,9 @@ uint64_t bulk_grid(uint64_t tiles, int resident)
 
 template <int KIND>
 struct BulkShape {
-    static constexpr int kStages = KIND == kStream ? 12 : KIND == kSplit ? 4 : KIND == kGather ? 6
-                                   : KIND == kWideSplit ? 3 : 2;
-    static constexpr int kTile = KIND == kStream || KIND == kSplit ? 16384
+    static constexpr int kStages = KIND == kStream ? 12 : KIND == kSplit || KIND == kGatherSplit ? 4
+                                   : KIND == kGather ? 6 : KIND == kWideSplit ? 3 : 2;
+    static constexpr int kTile = KIND == kStream || KIND == kSplit || KIND == kGatherSplit ? 16384
                                  : KIND == kGather || KIND == kWideSplit ? 32768 : 98304;
     static constexpr size_t kBarBytes = ((size_t)kStages * 8 + 127) / 128 * 128;
     static constexpr size_t kSmem = kBarBytes + (size_t)kStages * kTile;
@@ -327,6 +334,8 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
             return launch_bulk<NSEG, NOUT, kStream>(p, device, s);
         return launch_bulk<NSEG, NOUT, kSplit>(p, device, s);
     }
+    if (max_dst <= 8 && cut_tiles(p, BulkShape<kGatherSplit>::kTile) >= 3 * (uint64_t)sm_count(device))
+        return launch_bulk<NSEG, NOUT, kGatherSplit>(p, device, s);
     cut_tiles(p, BulkShape<kGather>::kTile);
     return launch_bulk<NSEG, NOUT, kGather>(p, device, s);
 }

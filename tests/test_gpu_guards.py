@@ -158,12 +158,14 @@ def test_all_to_all_writes_only_its_outputs(dt, P, chunk_bytes):
         assert_same(host(o.view(torch.uint8)), want[j], f"rank {j}")
 
 
-@pytest.mark.parametrize("P,chunk_bytes", [(16, 7 * 16384 + 48), (8, (2 << 20) + 48)])
+@pytest.mark.parametrize("P,chunk_bytes", [(16, 7 * 16384 + 48), (8, (2 << 20) + 48),
+                                           (4, (1 << 20) + 48)])
 def test_bulk_all_to_all_shapes_write_only_their_outputs(dt, P, chunk_bytes):
-    # The two bulk-copy shapes of an AllToAll of 8+ ranks, each segment ending
-    # in a 48-byte partial tile: 16 ranks of ~1.8 MiB (data fits in L2: four
-    # stages, three blocks per SM) and 8 ranks of ~16 MiB (data larger than
-    # half of L2: twelve stages, one block per SM).
+    # The bulk-copy shapes of an AllToAll, each segment ending in a 48-byte
+    # partial tile: 16 ranks of ~1.8 MiB (data fits in L2: four stages, three
+    # blocks per SM), 8 ranks of ~16 MiB (data larger than half of L2: twelve
+    # stages, one block per SM) and 4 ranks of ~4 MiB (16 segments: 16 KiB x
+    # 4 stages, three blocks per SM).
     gen = torch.Generator(device="cuda").manual_seed(P + chunk_bytes)
     xs = [torch.randint(0, 256, (P * chunk_bytes,), generator=gen, dtype=torch.uint8, device="cuda")
           for _ in range(P)]
