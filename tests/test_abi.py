@@ -108,3 +108,32 @@ def test_nvtx_flavour_compiles(tmp_path):
            os.path.join(b.CSRC, "dt_group.cpp"), "-o", str(tmp_path / "g.o")]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def test_prepared_calls_make_the_same_call_as_the_functions(dt):
+    # With a null group every entry point returns DT_ERR_INVALID before it
+    # looks at anything else, so the marshalled arguments can be exercised
+    # without a device (explicit stream handles; pointers are never read).
+    cases = [(dt.dt_allreduce, (None, -1, [16, 32], [48, 64], 16, "f32", "sum", 0, 7)),
+             (dt.dt_reduce_scatter, (None, -1, [16], [32], 4, "bf16", "avg", 7)),
+             (dt.dt_all_gather, (None, -1, [16], [32], [3], 0, 16, 0, 7)),
+             (dt.dt_all_to_all, (None, -1, [16], [32], 16, 7)),
+             (dt.dt_all_to_all_2d, (None, -1, [16], [32], 4, 4, 2, 0, 1, 7)),
+             (dt.dt_replicate_to_shard, (None, -1, [16], [32], None, 4, 16, 7)),
+             (dt.dt_all_gather_into_vec, (None, -1, [16], [32], None, 1, 16, 7)),
+             (dt.dt_barrier, (None, -1, 7)),
+             (dt.dt_bucket_allreduce, (None, [[16, 32]], [4], "f32", "avg", 0, 7))]
+    for fn, args in cases:
+        p = dt.prepare(fn, *args)
+        assert p.name == fn.__name__
+        for _ in range(2):                                  # reusable
+            with pytest.raises(dt.DtError) as e:
+                p()
+            assert e.value.status == dt.DT_ERR_INVALID, fn.__name__
+        with pytest.raises(dt.DtError) as e:
+            fn(*args)
+        assert e.value.status == dt.DT_ERR_INVALID, fn.__name__
+    with pytest.raises(ValueError):
+        dt.prepare(dt.dt_status_string, 0)
+    with pytest.raises(ValueError):
+        dt.prepare(print, 0)

@@ -248,3 +248,52 @@ def test_rank_local_chained_rounds_stay_ordered(dt, P):
     for r in range(P):
         assert_same(host(bufs[r]), host_b[r], f"rank {r}")
     assert np.array_equal(win, oracle.expected_window(P, int((kinds == "barrier").sum())))
+
+
+def test_prepared_calls_from_rank_threads(dt):
+    # The RS(avg) + AG step from four rank threads through prepared calls
+    # (arguments marshalled once, the same C call each step), three steps in a
+    # row, compared with the oracle; a prepared group-wide AllReduce matches
+    # the per-call function bit for bit.
+    P, rows, cols = 4, 64, 40
+    gen = torch.Generator().manual_seed(77)
+    xs = [torch.randn(rows, cols, generator=gen).to(torch.bfloat16).cuda() for _ in range(P)]
+    m = rows // P * cols
+    rs = [torch.empty(rows // P, cols, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ag = [torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    torch.cuda.synchronize()
+    with group(P) as g:
+        steps = []
+        for r in range(P):
+            raw = streams[r].cuda_stream
+            steps.append([dt.prepare(dt.dt_barrier, g, r, raw),
+                          dt.prepare(dt.dt_reduce_scatter, g, r, [xs[r]], [rs[r]], m, "bf16", "avg",
+                                     raw),
+                          dt.prepare(dt.dt_barrier, g, r, raw),
+                          dt.prepare(dt.dt_all_gather, g, r, [rs[r]], [ag[r]], None, rows // P,
+                                     cols * 2, 0, raw)])
+
+        def rank(r):
+            for _ in range(3):
+                for call in steps[r]:
+                    call()
+
+        assert run_ranks(P, rank) == [None] * P
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+        want_rs = oracle.reduce_scatter("bf16", "avg", [host(x) for x in xs])
+        want_ag = oracle.all_gather(want_rs)
+        for r in range(P):
+            assert_same(host(rs[r]), want_rs[r], f"reduce_scatter rank {r}")
+            assert_same(host(ag[r]), want_ag[r], f"all_gather rank {r}")
+        assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, 6))
+
+        a = [torch.empty_like(x) for x in xs]
+        b = [torch.empty_like(x) for x in xs]
+        s = torch.cuda.current_stream().cuda_stream
+        dt.prepare(dt.dt_allreduce, g, dt.DT_ALL_RANKS, xs, a, rows * cols, "bf16", "sum", 0, s)()
+        dt.dt_allreduce(g, dt.DT_ALL_RANKS, xs, b, rows * cols, "bf16", "sum", 0, s)
+        torch.cuda.synchronize()
+        for q in range(P):
+            assert_same(host(a[q]), host(b[q]), f"allreduce rank {q}")
