@@ -440,6 +440,13 @@ def measure_rows(dt, dev, peak, only=None):
         e.record()
         torch.cuda.synchronize()
         us_direct = s.elapsed_time(e) * 1e3 / calls
+        bar = dt.prepare(dt.dt_barrier, g, ALL, raw)     # the same call, marshalled once
+        s.record()
+        for _ in range(calls):
+            bar()
+        e.record()
+        torch.cuda.synchronize()
+        us_prepared = s.elapsed_time(e) * 1e3 / calls
         us_graph = None
         try:
             stream = torch.cuda.Stream(dev)
@@ -463,6 +470,7 @@ def measure_rows(dt, dev, peak, only=None):
         win_ok = dt.dt_group_check(g) == dt.DT_OK
         dt.dt_group_destroy(g)
         rows["barrier_P16"] = {"us_per_call_stream": round(us_direct, 3),
+                               "us_per_call_stream_prepared": round(us_prepared, 3),
                                "us_per_call_graph": us_graph if isinstance(us_graph, str)
                                else round(us_graph, 3), "calls": calls, "status_ok": win_ok}
 
