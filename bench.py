@@ -776,6 +776,8 @@ NCU_CASES = {
     "bucket": ("bucket_kernel", 14, "bucket AllReduce kAvg bf16, P=8, 200 tensors, 25 MiB buckets"),
     "all_to_all": ("copy_bulk_kernel", 2, "AllToAll bf16, P=8, [8192, 4096] per rank"),
     "all_to_all_p16": ("copy_bulk_kernel", 2, "AllToAll bf16, P=16, [8192, 2048] per rank"),
+    "reduce_scatter_max_p16": ("reduce_vec_kernel", 2,
+                               "ReduceScatter kMax bf16, P=16, 64 MiB per rank (sweep point)"),
     "uneven_all_gather": ("copy_bulk_kernel", 2,
                           "uneven AllGather int32, P=8, rows U[1, 2048] x 4096, per-rank outputs"),
     "barrier": ("barrier_kernel", 2, "signal-window barrier, P=16"),
@@ -814,6 +816,12 @@ def run_ncu_case(name):
         nbytes = w.inputs[0].numel() * 2
         g = dt.dt_group_create(16, dev.index)
         call = lambda: dt.dt_all_to_all(g, ALL, w.inputs, outs, nbytes // 16)
+    elif name == "reduce_scatter_max_p16":
+        w = workloads.sweep_inputs(4, 16, 64 << 20, "bf16", device=str(dev))
+        n = w.inputs[0].numel()
+        outs = [torch.empty(n // 16, dtype=torch.bfloat16, device=dev) for _ in range(16)]
+        g = dt.dt_group_create(16, dev.index)
+        call = lambda: dt.dt_reduce_scatter(g, ALL, w.inputs, outs, n // 16, "bf16", "max")
     elif name == "uneven_all_gather":
         w = workloads.uneven_gather(max_rows=2048, device=str(dev))
         rws = w.meta["rows"]
