@@ -957,7 +957,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, el, reps = time_oracle(1024, min_seconds=10.0, max_reps=50)
+        v, el, reps = time_oracle(1024, min_seconds=10.0, max_reps=400)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"RS(avg)+AG on {P} ranks x bf16 [1024, {COLS}] (1/8 of the workload's "
                          f"rows, drawn with the same recipe), {reps} reps in {el:.1f} s, "
