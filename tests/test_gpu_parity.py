@@ -482,3 +482,54 @@ def test_invalid_arguments_are_rejected_without_launch(dt):
         torch.cuda.synchronize()
         assert all(bool((t == -7.25).all()) for t in o + vec)
         assert dt.dt_group_check(g) == dt.DT_OK
+
+
+# --------------------------------------------------- every rank count 1..16
+@pytest.mark.parametrize("P", list(range(1, 17)))
+def test_every_rank_count(dt, P):
+    # Each P from 1 to 16 (the kernels are compiled for at most 2, 4, 8 and 16
+    # ranks and take the first P): AllReduce and ReduceScatter with the
+    # special-value MAX/MIN inputs and with sums, an AllToAll whose P^2 chunks
+    # of 48 KiB + 16 B go through the bulk copy, and an uneven AllGather.
+    m = 1031                                                  # ragged vector tail
+    for dtype, op in [("f32", "max"), ("bf16", "min"), ("bf16", "avg"), ("i32", "sum")]:
+        if op in ("max", "min"):
+            bits = _special_bits(dtype, P, P * m, 500 + P)
+            xs = [_device_from_bits(b, dtype) for b in bits]
+        else:
+            xs = rand_inputs(P, P * m, dtype, 600 + P)
+        outs = [torch.empty_like(x) for x in xs]
+        shards = [torch.empty(m, dtype=TORCH_DTYPE[dtype], device="cuda") for _ in range(P)]
+        with group(P) as g:
+            dt.dt_allreduce(g, dt.DT_ALL_RANKS, xs, outs, P * m, dtype, op)
+            dt.dt_reduce_scatter(g, dt.DT_ALL_RANKS, xs, shards, m, dtype, op)
+            torch.cuda.synchronize()
+        hx = [host(x) for x in xs]
+        want = oracle.allreduce(dtype, op, hx)
+        for q in range(P):
+            assert_same(host(outs[q]), want[q], f"{dtype} {op} allreduce rank {q}")
+        want = oracle.reduce_scatter(dtype, op, hx)
+        for r in range(P):
+            assert_same(host(shards[r]), want[r], f"{dtype} {op} reduce_scatter rank {r}")
+
+    chunk = 48 * 1024 + 16
+    gen = torch.Generator(device="cuda").manual_seed(700 + P)
+    xs = [torch.randint(0, 256, (P * chunk,), generator=gen, dtype=torch.uint8, device="cuda")
+          for _ in range(P)]
+    a2a = [torch.empty_like(x) for x in xs]
+    rows = [int(v) for v in torch.randint(0, 300, (P,), generator=torch.Generator().manual_seed(P))]
+    row_bytes = 4096
+    shard = [torch.randint(0, 256, (c * row_bytes,), generator=gen, dtype=torch.uint8, device="cuda")
+             for c in rows]
+    ag = [torch.empty(sum(rows) * row_bytes, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    with group(P) as g:
+        dt.dt_all_to_all(g, dt.DT_ALL_RANKS, xs, a2a, chunk)
+        dt.dt_all_gather(g, dt.DT_ALL_RANKS, shard, ag, rows, 0, row_bytes)
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+    want = oracle.all_to_all([host(x) for x in xs])
+    for j in range(P):
+        assert_same(host(a2a[j]), want[j], f"all_to_all rank {j}")
+    want = oracle.all_gather([host(s) for s in shard], rows, row_bytes)
+    for q in range(P):
+        assert_same(host(ag[q]), want[q], f"all_gather rank {q}")
