@@ -16,6 +16,8 @@
 // stores carry an evict-first L2 policy: their dirty lines leave L2 early
 // instead of being written back during the next kernel.  Anything else takes
 // a byte-wise kernel with the same tiling.
+#include <atomic>
+
 #include "dt_internal.h"
 #include "dt_device.cuh"
 
@@ -241,13 +243,17 @@ cudaError_t launch_bulk(const CopyParams<NSEG, NOUT> &p, int device, cudaStream_
 {
     using Shape = BulkShape<KIND>;
     void (*fn)(CopyParams<NSEG, NOUT>) = copy_bulk_kernel<NSEG, NOUT, KIND>;
-    static bool attr_set = false;   // per instantiation; the attribute is per function
-    if (!attr_set) {
+    // The shared-memory opt-in is an attribute of the function on the current
+    // device: set it once per device (bit `device` of this instantiation's mask;
+    // setting it twice from racing threads is harmless).
+    static std::atomic<uint64_t> attr_set{0};
+    const uint64_t bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Shape::kSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set.fetch_or(bit, std::memory_order_release);
     }
     int resident = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBulkThreads, device,
