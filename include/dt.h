@@ -76,7 +76,7 @@ typedef struct dt_work *dt_work_t;
 typedef enum {
     DT_OK = 0,
     DT_ERR_INVALID = 1,      /* bad argument; nothing was enqueued */
-    DT_ERR_UNSUPPORTED = 2,  /* legal request this build does not do (AVG on int32, ...) */
+    DT_ERR_UNSUPPORTED = 2,  /* legal request the library does not support (AVG on int32, ...) */
     DT_ERR_CUDA = 3,         /* a CUDA runtime call failed */
     DT_ERR_TIMEOUT = 4,      /* a device-side wait ran out of time (see dt_group_check) */
     DT_ERR_OOM = 5,          /* the group could not allocate its own state */
