@@ -66,6 +66,25 @@ bool log_enabled()
     return on;
 }
 
+bool debug_enabled()
+{
+    static const bool on = [] {
+        const char *env = std::getenv("DT_DEBUG");
+        return env && env[0] && env[0] != '0';
+    }();
+    return on;
+}
+
+cudaError_t debug_sync(cudaStream_t s, cudaError_t launched)
+{
+    if (launched != cudaSuccess) return launched;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) return cudaSuccess;   // nothing runs while capturing
+    return cudaStreamSynchronize(s);
+}
+
 void log_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool cooperative,
                 cudaError_t result)
 {

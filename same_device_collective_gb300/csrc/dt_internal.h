@@ -157,6 +157,12 @@ bool pdl_enabled();
 // DT_LOG=1 in the environment: every launch prints its kernel, grid, block,
 // dynamic shared memory, stream and launch attributes to stderr.
 bool log_enabled();
+
+// DT_DEBUG=1 in the environment: every launch is followed by a synchronisation
+// of its stream (skipped while the stream is being captured), so a kernel that
+// fails is reported by the call that launched it rather than by a later one.
+bool debug_enabled();
+cudaError_t debug_sync(cudaStream_t s, cudaError_t launched);
 void log_launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool cooperative,
                 cudaError_t result);
 
@@ -186,7 +192,7 @@ cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t s
     count_launch();
     const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
     if (log_enabled()) log_launch(reinterpret_cast<const void *>(fn), grid, block, smem, s, cooperative, e);
-    return e;
+    return debug_enabled() ? debug_sync(s, e) : e;
 }
 int sm_count(int device);
 // Bytes of L2 cache on the device (cached per device).

@@ -55,3 +55,10 @@ def test_no_output_without_dt_log():
     res = run({"DT_LOG": "0"})
     assert res.returncode == 0, res.stderr[-2000:]
     assert not [l for l in res.stderr.splitlines() if l.startswith("dt: ")]
+
+
+def test_dt_debug_synchronises_every_launch_and_results_hold():
+    # DT_DEBUG=1: each launch is followed by a synchronisation of its stream;
+    # the same script (barrier, AllReduce, two bucket calls) still succeeds.
+    res = run({"DT_DEBUG": "1", "DT_LOG": "0"})
+    assert res.returncode == 0, res.stderr[-2000:]
