@@ -102,6 +102,15 @@ typedef enum { DT_SUM = 0, DT_AVG = 1, DT_MAX = 2, DT_MIN = 3, DT_SUM_STEPWISE =
 /* Default bucket cap: DDP's bucket_cap_mb = 25, read as 25 MiB. */
 #define DT_DEFAULT_BUCKET_CAP_BYTES ((size_t)25 << 20)
 
+/* Environment switches, read once per process:
+ *   DT_TIMEOUT_MS  limit of every device wait and host rendezvous, in ms
+ *                  (default 2000; read by dt_group_create)
+ *   DT_LOG=1       every kernel launch and bucket plan is printed to stderr
+ *   DT_PDL=0       kernels are launched without programmatic dependent launch
+ *   DT_DEBUG=1     every launch is followed by a synchronisation of its stream
+ *                  (not while the stream is being captured), so a kernel that
+ *                  fails is reported by the call that launched it */
+
 /* ------------------------------------------------------------------ groups */
 
 /* Create a group of world_size (1..DT_MAX_RANKS) logical ranks on CUDA device
