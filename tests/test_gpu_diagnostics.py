@@ -62,3 +62,12 @@ def test_dt_debug_synchronises_every_launch_and_results_hold():
     # the same script (barrier, AllReduce, two bucket calls) still succeeds.
     res = run({"DT_DEBUG": "1", "DT_LOG": "0"})
     assert res.returncode == 0, res.stderr[-2000:]
+
+
+def test_launches_without_programmatic_dependent_launch():
+    # DT_PDL=0: every kernel is launched with plain stream ordering; the same
+    # script still succeeds.
+    res = run({"DT_PDL": "0", "DT_LOG": "1"})
+    assert res.returncode == 0, res.stderr[-2000:]
+    launches = [l for l in res.stderr.splitlines() if l.startswith("dt: launch ")]
+    assert launches and all(l.endswith("-> cudaSuccess") for l in launches)
