@@ -275,9 +275,10 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
 /* Allocation-free fused bucket all-reduce.  The pages have no counterpart:
  * this entry point exists for callers that cannot let a library allocate
  * device memory -- applications that own all device memory through their own
- * pool (cudaMalloc synchronises the device and escapes their accounting) and
- * code running while a global-mode stream capture is active, where cudaMalloc
- * is not permitted.  Such callers cannot create a dt_group.
+ * pool (a library's cudaMalloc escapes their accounting and can fail once the
+ * pool has taken the device) and code on a latency-critical path that must
+ * not stall other streams (cudaMalloc and cudaFree can synchronise the whole
+ * device).  Such callers cannot create a dt_group.
  *   world_size        P (1..DT_MAX_RANKS); no group is needed
  *   grads, counts, n_tensors, dtype, op, bucket_cap_bytes, stream
  *                     as dt_bucket_allreduce; the results are identical

@@ -1,10 +1,11 @@
 // Allocation-free variant of the fused bucket all-reduce.
 //
 // Some callers cannot let a library call cudaMalloc: applications that own
-// all device memory through their own pool (cudaMalloc synchronises the
-// device and bypasses their accounting), and code that runs while a stream
-// capture in global mode is active, where cudaMalloc is not permitted.  They
-// cannot create a dt_group, which allocates its window and plan scratch.
+// all device memory through their own pool (a library's cudaMalloc bypasses
+// their accounting and can fail once the pool has taken the device), and code
+// on a latency-critical path that must not stall the other streams
+// (cudaMalloc and cudaFree can synchronise the whole device).  They cannot
+// create a dt_group, which allocates its window and plan scratch.
 // dt_bucket_allreduce_static serves them: the tensor and pointer tables that
 // the bucket kernel reads live in a fixed file-scope device array of
 // kStaticScratchBytes, staged from a fixed host array, so a call allocates

@@ -1,9 +1,10 @@
 """The allocation-free bucket all-reduce gives the group-based one's results.
 
 dt_bucket_allreduce_static is for callers that cannot let a library allocate
-device memory: applications whose own pool owns all device memory (cudaMalloc
-would synchronise the device and escape their accounting) and code running
-while a global-mode stream capture is active, where cudaMalloc is not allowed.
+device memory: applications whose own pool owns all device memory (a
+library's cudaMalloc would escape their accounting and can fail once the pool
+has taken the device) and code on a latency-critical path that must not stall
+other streams (cudaMalloc and cudaFree can synchronise the whole device).
 It keeps its tables in one fixed device array inside the library instead of a
 group's scratch.  These tests call it through the C ABI and compare its output
 with dt_bucket_allreduce's, bit for bit (the tolerance of every parity test
