@@ -291,10 +291,18 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
  * buckets) or more than 4096 buckets return DT_ERR_TOO_LARGE before anything
  * is enqueued.  Every call shares the array and leaves its contents behind;
  * calls that overlap on the GPU (unordered streams) race on it, calls on one
- * stream do not.  No signal barrier runs between buckets (there is no group
+ * stream do not.  A call whose tables differ from the last ones copied to
+ * this device copies them with a pageable cudaMemcpyAsync, which CUDA may
+ * finish only after the work already queued on `stream`, so such a call can
+ * block the host until then; a call that repeats the previous call's
+ * gradients, counts, dtype, cap and ranks on the same device finds its
+ * tables there and neither copies nor waits.  A call on a stream that is
+ * being captured returns DT_ERR_UNSUPPORTED and enqueues nothing (a captured
+ * copy would read the host array at replay time, after later calls have
+ * rewritten it).  No signal barrier runs between buckets (there is no group
  * window); stream order orders them.  The first call on each device looks up
- * the array's device address with that device current: make it before any
- * stream capture begins.  The current CUDA device must be the gradients'. */
+ * the array's device address with that device current.  The current CUDA
+ * device must be the gradients'. */
 dt_status dt_bucket_allreduce_static(int world_size, void *const *grads, const size_t *counts,
                                      size_t n_tensors, int dtype, int op,
                                      size_t bucket_cap_bytes, void *stream);

@@ -14,13 +14,21 @@
 // Costs and rules of the fixed array:
 //   - every GPU that loads this library holds the array (1 MiB) until the
 //     process exits;
-//   - every call shares it and it keeps the last call's contents; each call
-//     overwrites the part it uses before its kernels read it;
+//   - every call shares it and it keeps the last call's contents; a call
+//     whose tables differ from the last ones copied to its device overwrites
+//     the part it uses before its kernels read it, and a call that repeats
+//     them (same device, ranks, dtype, cap, gradients and counts) reuses them
+//     without a copy;
 //   - calls that overlap on the GPU (issued on different streams without
 //     ordering between them) race on the array; calls on one stream are safe;
+//   - the copy is from pageable host memory, which CUDA may complete only
+//     after the work already queued on the stream: a call that copies can
+//     block the host until then, a call that reuses the tables does not;
+//   - a call on a stream that is being captured is refused (the copy would
+//     be recorded as reading the host array at replay time, after later
+//     calls have rewritten it);
 //   - the first call on each device looks up the array's device address
-//     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture begins.
+//     (cudaGetSymbolAddress) with that device current.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -44,6 +52,23 @@ namespace {
 // Host staging of the same size: copied with a pageable cudaMemcpyAsync,
 // which returns once the bytes have left this array.
 alignas(256) unsigned char h_bucket_staging[kStaticScratchBytes];
+// What the last copy put on the device: its bytes and the arguments they
+// encode.  A call that builds the same bytes for the same device, ranks,
+// dtype and cap finds them there already.
+alignas(256) unsigned char h_last_upload[kStaticScratchBytes];
+struct UploadKey {
+    int device = -1;
+    int P = 0;
+    int dtype = -1;
+    size_t bytes = 0;
+};
+UploadKey g_last_key;
+// Gradient byte ranges for the overlap check: every range takes at least one
+// 8-byte pointer of the table, so the table's limit bounds their number.
+struct GradRange {
+    uintptr_t lo, hi;
+};
+GradRange h_ranges[kStaticScratchBytes / sizeof(void *)];
 std::mutex g_static_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
@@ -89,16 +114,10 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
             if (!grads[t * P + p]) return DT_ERR_INVALID;
     }
 
-    // no two gradient buffers may overlap: quadratic check, no allocation
-    for (size_t t = 0; t < n_tensors; ++t)
-        for (int p = 0; p < P && counts[t]; ++p) {
-            const uintptr_t lo = (uintptr_t)grads[t * P + p], hi = lo + counts[t] * es;
-            for (size_t u = t; u < n_tensors; ++u)
-                for (int q = (u == t ? p + 1 : 0); q < P && counts[u]; ++q) {
-                    const uintptr_t lo2 = (uintptr_t)grads[u * P + q], hi2 = lo2 + counts[u] * es;
-                    if (lo < hi2 && lo2 < hi) return DT_ERR_INVALID;
-                }
-        }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) return DT_ERR_CUDA;
+    if (capture != cudaStreamCaptureStatusNone) return DT_ERR_UNSUPPORTED;
 
     std::lock_guard<std::mutex> lock(g_static_mu);
     int device = 0;
@@ -159,13 +178,37 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     }
     if (nl == 0) return DT_OK;
 
+    const size_t plan_bytes = ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t);
+    const bool reuse = g_last_key.device == device && g_last_key.P == P && g_last_key.dtype == dtype &&
+                       g_last_key.bytes == plan_bytes &&
+                       memcmp(h_last_upload, h_bucket_staging, plan_bytes) == 0;
+    if (!reuse) {
+        // No two gradient buffers may overlap: sort their byte ranges and
+        // compare neighbours (the first overlap in start order is always
+        // between neighbours).  A call that repeats the last tables was
+        // checked when they were copied.
+        size_t nr = 0;
+        for (size_t t = 0; t < n_tensors; ++t)
+            for (int p = 0; p < P && counts[t]; ++p) {
+                const uintptr_t lo = (uintptr_t)grads[t * P + p];
+                h_ranges[nr++] = GradRange{lo, lo + counts[t] * es};
+            }
+        std::sort(h_ranges, h_ranges + nr,
+                  [](const GradRange &a, const GradRange &b) { return a.lo < b.lo; });
+        for (size_t i = 1; i < nr; ++i)
+            if (h_ranges[i].lo < h_ranges[i - 1].hi) return DT_ERR_INVALID;
+    }
+
     void *scratch = nullptr;
     if (scratch_address(device, &scratch) != cudaSuccess) return DT_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(scratch, h_bucket_staging,
-                                    ptr_bytes + tab_bytes + n_starts * sizeof(uint32_t),
-                                    cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return DT_ERR_CUDA;
+    if (!reuse) {
+        g_last_key = UploadKey{};   // the device copy is in flux until this copy is queued
+        if (cudaMemcpyAsync(scratch, h_bucket_staging, plan_bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return DT_ERR_CUDA;
+        memcpy(h_last_upload, h_bucket_staging, plan_bytes);
+        g_last_key = UploadKey{device, P, dtype, plan_bytes};
+    }
 
     const unsigned char *d = static_cast<const unsigned char *>(scratch);
     dt::BucketParams bp;
