@@ -247,9 +247,12 @@ dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *
  *   bucket_cap_bytes  0 -> DT_DEFAULT_BUCKET_CAP_BYTES
  * Tensors are grouped in order into buckets (dt_bucket_plan); each bucket is
  * one kernel that reads and writes the gradients in place through a chunk
- * table (no flatten copy), and one signal-window barrier (dt_barrier) runs
- * between consecutive buckets.  The plan table is staged through the group's
- * scratch; at most one bucket call per group may be in flight. */
+ * table (no flatten copy), and one signal-window barrier (the notify / wait
+ * of dt_barrier, one generation each) runs between consecutive buckets: in an
+ * extra last block of the earlier bucket's kernel, which waits until that
+ * bucket's other blocks have finished.  The next bucket's kernel starts once
+ * that whole kernel has completed.  The plan table is staged through the
+ * group's scratch; at most one bucket call per group may be in flight. */
 dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *counts,
                               size_t n_tensors, int dtype, int op, size_t bucket_cap_bytes,
                               void *stream);
@@ -286,8 +289,8 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
  * this library (every GPU that loads the library holds it until the process
  * exits) and are staged from a fixed host array: the call allocates nothing.
  * Tables that do not fit (n_tensors * (P * 8 + 24) bytes plus 4 bytes per
- * thread block of every bucket: one block per 2048 bf16 or 1024 fp32
- * elements, at most 16 per resident block slot, so about 40 full 25 MiB
+ * thread block of every bucket: one block per 1024 bf16 or 512 fp32
+ * elements, at most 16 per resident block slot, so about 20 full 25 MiB
  * buckets) or more than 4096 buckets return DT_ERR_TOO_LARGE before anything
  * is enqueued.  Every call shares the array and leaves its contents behind;
  * calls that overlap on the GPU (unordered streams) race on it, calls on one

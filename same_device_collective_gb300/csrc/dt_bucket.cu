@@ -23,8 +23,97 @@ struct BucketUnroll {   // 8 loads of 16 bytes in flight per thread (16 at P > 8
     static constexpr int U = PMAX >= 8 ? 1 : 8 / PMAX;
 };
 
+// Threads per bucket block.  Blocks make one pass over their slice, so the
+// block size sets the slice and with it how long the last blocks of a bucket
+// run alone at its end: 128 threads measured 384 -> 380 us per call on the
+// 200-gradient, 8-rank workload against 256 (64: no further gain).
+constexpr int kBucketThreads = 128;
+
+// The signal-window barrier between this bucket and the next, run by the
+// grid's extra last block (the page's notify / wait with a generation; the
+// stand-alone form is barrier_kernel, one warp per rank).  The data blocks
+// count themselves out in the group's finished-block counter as they end;
+// this block, dispatched after all of them, waits for the previous kernel,
+// then until the count is complete, resets it for the next bucket kernel, and
+// then acts for all P
+// ranks at once: thread cell (r, q) adds 1 to row r of peer q's window (rank
+// r's notify, AtomicAdd) and then waits until row q of rank r's window
+// reaches rank r's generation (Ge).  The next kernel starts after this grid
+// has completed, so it sees every gradient this bucket wrote, as it would
+// after a barrier kernel -- whose own launch-to-completion hop is what this
+// saves at every bucket boundary.  Every wait is bounded: one that runs out
+// records DT_ERR_TIMEOUT and ends the block.
+__device__ void bucket_barrier_block(const BucketParams &p)
+{
+    __shared__ int ok;
+    const int P = p.P;
+    int32_t *rank_gen = p.win + P * P;
+    uint32_t *done = reinterpret_cast<uint32_t *>(rank_gen + P);
+    // The previous kernel may still be running (this grid was launched while
+    // it drained): it may be a bucket kernel whose own blocks are still
+    // counting themselves out and whose barrier block has yet to update the
+    // window.  Touch neither before it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        ok = 1;
+        const uint32_t others = gridDim.x - 1;
+        const uint64_t t0 = global_ns();
+        const uint64_t max_polls = p.sink.timeout_ns / 64 + 4096;
+        for (uint64_t it = 0;; ++it) {
+            uint32_t v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(done) : "memory");
+            if (v >= others) break;
+            if (it >= max_polls || global_ns() - t0 > p.sink.timeout_ns) {
+                record_error(p.sink, DT_ERR_TIMEOUT, -1, -1, 0);
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (ok) asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(done), "r"(0u) : "memory");
+    }
+    __syncthreads();
+    if (!ok) return;
+    for (int c = threadIdx.x; c < P * P; c += blockDim.x) {
+        const int r = c / P, q = c - r * P;
+        if (r != q) asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(&p.win[q * P + r]), "r"(1) : "memory");
+    }
+    for (int c = threadIdx.x; c < P * P; c += blockDim.x) {
+        const int r = c / P, s = c - r * P;
+        if (r == s) continue;
+        const int32_t g = rank_gen[r] + 1;
+        const int32_t *cell = &p.win[r * P + s];
+        const uint64_t t0 = global_ns();
+        const uint64_t max_polls = p.sink.timeout_ns / 64 + 4096;
+        for (uint64_t it = 0;; ++it) {
+            int32_t v;
+            asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cell) : "memory");
+            if ((int32_t)(v - g) >= 0) break;             // Ge, safe across wrap-around
+            if (it >= max_polls || global_ns() - t0 > p.sink.timeout_ns) {
+                record_error(p.sink, DT_ERR_TIMEOUT, r, s, g);
+                break;
+            }
+            if (it >= 64) __nanosleep(128);
+        }
+    }
+    __syncthreads();   // every rank has read its generation and passed its wait
+    if (threadIdx.x < P) rank_gen[threadIdx.x] += 1;
+}
+
+// A data block of a bucket followed by a barrier counts itself out.  The
+// barrier block only needs to know that every data block has finished its
+// work: the next kernel waits for this whole grid before it reads anything.
+__device__ __forceinline__ void count_out(const BucketParams &p)
+{
+    if (!p.win) return;
+    __syncthreads();
+    if (threadIdx.x == 0)
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;"
+                     ::"l"(p.win + p.P * p.P + p.P), "r"(1u) : "memory");
+}
+
 template <int DT, int OP, int PMAX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kBucketThreads)
 bucket_kernel(const __grid_constant__ BucketParams p)
 {
     constexpr int U = BucketUnroll<PMAX>::U;
@@ -38,9 +127,14 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     // gradients themselves are touched only after griddepcontrol.wait.  This
     // takes two dependent table reads off the start of every bucket.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.win && blockIdx.x == gridDim.x - 1) {
+        bucket_barrier_block(p);
+        return;
+    }
     const uint64_t lo = (uint64_t)blockIdx.x * p.per_block;
     if (lo >= p.total) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        count_out(p);
         return;
     }
     const uint64_t hi = lo + p.per_block < p.total ? lo + p.per_block : p.total;
@@ -58,11 +152,11 @@ bucket_kernel(const __grid_constant__ BucketParams p)
             uint64_t scalar_from = s;
             if (bt.slot >> 31) {
                 const uint64_t vs = s / EPV, ve = e / EPV;   // s is a multiple of EPV
-                for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kThreads * U) {
+                for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kBucketThreads * U) {
                     uint4 x[U][PMAX];
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const uint64_t v = base + (uint64_t)u * kThreads;
+                        const uint64_t v = base + (uint64_t)u * kBucketThreads;
                         if (v < ve) {
 #pragma unroll
                             for (int r = 0; r < PMAX; ++r)
@@ -71,7 +165,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                     }
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const uint64_t v = base + (uint64_t)u * kThreads;
+                        const uint64_t v = base + (uint64_t)u * kBucketThreads;
                         if (v < ve) {
                             const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
 #pragma unroll
@@ -82,7 +176,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                 }
                 scalar_from = ve * EPV;   // ragged end of the tensor, if it is in this slice
             }
-            for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kThreads)
+            for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kBucketThreads)
                 reduce_elem<DT, OP>(sp, 0, i, P, sp, P, p.avg_scale, p.avg_pow2);
         }
         if (++t >= p.ntensors) break;
@@ -92,6 +186,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
         if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)(bt.slot & 0x7FFFFFFFu) * P + threadIdx.x];
         __syncthreads();
     }
+    count_out(p);
 }
 
 using BucketFn = void (*)(BucketParams);
@@ -127,11 +222,11 @@ cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, ui
     BucketFn fn = pick_fn(dtype, op, P);
     if (!fn) return cudaErrorInvalidValue;
     int resident = 0;
-    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
+    cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kBucketThreads, device, &resident);
     if (e != cudaSuccess) return e;
     const uint64_t epv = dtype == DT_BF16 ? 8 : 4;
     // at least one full pass of the block's threads per slice
-    const uint64_t min_slice = (uint64_t)kThreads * epv;
+    const uint64_t min_slice = (uint64_t)kBucketThreads * epv;
     uint64_t g = (total + min_slice - 1) / min_slice;
     // Up to sixteen slices per resident block: blocks that finish early take
     // the next slices, so SMs that stream slower do not stretch the bucket's
@@ -152,14 +247,19 @@ cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, ui
     return cudaSuccess;
 }
 
-cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s)
+cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s,
+                          bool *launched)
 {
+    if (launched) *launched = false;
     BucketFn fn = pick_fn(dtype, op, p.P);
     if (!fn) return cudaErrorInvalidValue;
     if (p.total == 0 || p.ntensors == 0) return cudaSuccess;
     (void)device;
-    const unsigned gx = (unsigned)((p.total + p.per_block - 1) / p.per_block);
-    return launch_kernel(fn, dim3(gx), dim3(kThreads), 0, s, false, p);
+    // data blocks, plus the barrier block when a barrier follows the bucket
+    const unsigned gx = (unsigned)((p.total + p.per_block - 1) / p.per_block) + (p.win ? 1u : 0u);
+    const cudaError_t e = launch_kernel(fn, dim3(gx), dim3(kBucketThreads), 0, s, false, p);
+    if (launched) *launched = e == cudaSuccess;
+    return e;
 }
 
 }  // namespace dt

@@ -518,7 +518,7 @@ dt_status dt_group_create(int world_size, int cuda_device, dt_group_t *out)
         const long v = std::strtol(env, nullptr, 10);
         if (v >= 1 && v <= 3600000) g->timeout_ms = (uint32_t)v;
     }
-    const size_t win_bytes = ((size_t)world_size * world_size + world_size) * sizeof(int32_t);
+    const size_t win_bytes = dt::win_words(world_size) * sizeof(int32_t);
     cudaError_t e = cudaMalloc(&g->d_win, win_bytes);
     if (e == cudaSuccess) e = cudaMemset(g->d_win, 0, win_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_err, sizeof(DevError));
@@ -571,7 +571,7 @@ dt_status dt_group_reset(dt_group_t g, void *stream)
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t win_bytes = ((size_t)g->P * g->P + g->P) * sizeof(int32_t);
+    const size_t win_bytes = dt::win_words(g->P) * sizeof(int32_t);
     cudaError_t e = cudaMemsetAsync(g->d_win, 0, win_bytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(g->d_err, 0, sizeof(DevError), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -1034,9 +1034,14 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     const size_t ptr_bytes = sl.ptr_bytes, tab_bytes = sl.tab_bytes;
     const std::vector<dt_group::PlanLaunch> &bl = sl.launches;
     dt::BucketParams bp;
+    memset(&bp, 0, sizeof bp);
     bp.ptrs = reinterpret_cast<void *const *>(d);
     bp.P = P;
     set_avg(P, &bp.avg_scale, &bp.avg_pow2);
+    bp.sink = error_sink(g);
+    // The barrier between buckets b and b + 1 runs in an extra last block of
+    // bucket b's kernel (the buckets' data decides nothing about it, so an
+    // empty bucket still gets its barrier from a kernel of its own).
     for (size_t b = 0; b < bl.size(); ++b) {
         const dt_group::PlanLaunch &L = bl[b];
         bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
@@ -1044,11 +1049,18 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         bp.ntensors = (uint32_t)(L.te - L.tb);
         bp.total = L.total;
         bp.per_block = L.per_block;
-        e = dt::launch_bucket(bp, dtype, op, g->device, s);
+        const bool barrier_after = b + 1 < bl.size();
+        bp.win = barrier_after ? g->d_win : nullptr;
+        bool launched = false;
+        e = dt::launch_bucket(bp, dtype, op, g->device, s, &launched);
         if (e != cudaSuccess) break;
-        if (b + 1 < bl.size()) {
-            st = issue_barrier(g, s);
-            if (st != DT_OK) return st;
+        if (barrier_after) {
+            if (launched) {
+                g->barriers_issued++;
+            } else {
+                st = issue_barrier(g, s);
+                if (st != DT_OK) return st;
+            }
         }
     }
     cudaError_t e2 = capturing ? cudaSuccess : cudaEventRecord(sl.done, s);

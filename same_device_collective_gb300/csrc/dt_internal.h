@@ -120,7 +120,17 @@ struct BucketParams {
     int32_t P;
     float avg_scale;
     int32_t avg_pow2;
+    // The signal-window barrier after this bucket, run by one extra block at
+    // the end of the grid (win != nullptr; see bucket_kernel): the group's
+    // window [P][P], followed by rank_gen[P] and the counter of finished
+    // blocks.
+    int32_t *win;
+    ErrorSink sink;
 };
+
+// Words of a group's barrier state: the window [P][P], the generations of the
+// ranks [P], the bucket kernels' finished-block counter, padding.
+constexpr size_t win_words(int P) { return (size_t)P * P + P + 4; }
 
 // Elements a tensor occupies in the flattened space, and the grid the bucket
 // kernel uses for `total` such elements (blocks the SMs hold at once).
@@ -209,7 +219,10 @@ cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nou
                         const ErrorSink &sink, int device, cudaStream_t s);
 cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, bool vec, int device,
                           cudaStream_t s);
-cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s);
+// *launched (optional) tells whether a kernel went out: a bucket with no
+// elements launches nothing, and then runs no barrier either.
+cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s,
+                          bool *launched = nullptr);
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s);
 cudaError_t launch_ring(const RingParams &p, cudaStream_t s);
 

@@ -212,6 +212,7 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
 
     const unsigned char *d = static_cast<const unsigned char *>(scratch);
     dt::BucketParams bp;
+    memset(&bp, 0, sizeof bp);   // gen = 0: no barrier between buckets
     bp.ptrs = reinterpret_cast<void *const *>(d);
     bp.P = P;
     bp.avg_pow2 = (P & (P - 1)) == 0;

@@ -190,7 +190,7 @@ def test_static_bucket_allreduce_rejects_tables_past_the_fixed_array(dt):
 
 def test_static_bucket_allreduce_full_workload(dt):
     # The 200-gradient, 8-rank bf16 workload (7 buckets of up to 25 MiB): its
-    # tables (about 200 KB with one-pass bucket slices) fit the fixed array,
+    # tables (about 400 KB with one-pass bucket slices) fit the fixed array,
     # and the result equals the group-based call's and the oracle's, bit for
     # bit (the oracle on 20 of the 200 gradients, spread over every bucket).
     from same_device_collective_gb300 import workloads as wl
