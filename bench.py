@@ -315,7 +315,7 @@ def time_events(fn, iters, warmup=3, lead_cycles=4_000_000, reps=1):
 
 
 ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "uneven_all_gather",
-             "barrier", "rank_local", "placements", "hsdp_pipeline"]
+             "barrier", "rank_local", "placements", "hsdp_pipeline", "sweep_points", "misaligned"]
 
 
 def measure_rows(dt, dev, peak, only=None):
@@ -703,6 +703,116 @@ def measure_rows(dt, dev, peak, only=None):
             "comm_GB/s_sequential_excl_compute": round(comm_bytes / max(t_seq - t_gemm, 1e-9) / 1e9, 1),
             "status_ok": ok, "timing": "wall clock, median of 5, synchronised"}
         del grads, rsb, fin, a, b, c
+
+    # Size sweep (config 5) at the message sizes the HBM target is stated
+    # for: every op at P = 2 and P = 16, bf16 kSum, 64 MiB and 256 MiB per
+    # rank, per-rank outputs; seeded uniform [-1, 1) inputs drawn on the
+    # device.  Timed like the other rows (8 back-to-back calls per sample).
+    if want("sweep_points"):
+        torch.cuda.empty_cache()
+        points = {}
+        for P in (2, 16):
+            g = dt.dt_group_create(P, dev.index)
+            for nbytes in (64 << 20, 256 << 20):
+                gen = torch.Generator(device=dev).manual_seed(4)
+                n = nbytes // 2
+                xs = [(torch.rand(n, generator=gen, device=dev) * 2 - 1).to(torch.bfloat16)
+                      for _ in range(P)]
+                outs = [torch.empty_like(x) for x in xs]
+                res = {}
+                ms = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "bf16", "sum"), 5,
+                                 reps=STEADY_REPS)
+                res["allreduce"] = (2 * P * nbytes, ms)
+                rs = [torch.empty(n // P, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+                ms = time_events(lambda: dt.dt_reduce_scatter(g, ALL, xs, rs, n // P, "bf16", "sum"), 5,
+                                 reps=STEADY_REPS)
+                res["reduce_scatter"] = ((P + 1) * nbytes, ms)
+                del rs
+                ms = time_events(lambda: dt.dt_all_to_all(g, ALL, xs, outs, nbytes // P), 5,
+                                 reps=STEADY_REPS)
+                res["all_to_all"] = (2 * P * nbytes, ms)
+                del outs
+                ag = [torch.empty(P * n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+                ms = time_events(lambda: dt.dt_all_gather(g, ALL, xs, ag, None, 1, nbytes), 5,
+                                 reps=STEADY_REPS)
+                res["all_gather"] = ((P + P * P) * nbytes, ms)
+                del ag, xs
+                torch.cuda.empty_cache()
+                for op, (b, t) in res.items():
+                    gbs = b / (t * 1e-3) / 1e9
+                    points[f"{op}_P{P}_{nbytes >> 20}MiB"] = {
+                        "GB/s": round(gbs, 1), "us": round(t * 1e3, 2),
+                        "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                        "frac_of_measured_hbm": round(gbs / peak, 4)}
+            assert dt.dt_group_check(g) == dt.DT_OK
+            dt.dt_group_destroy(g)
+        fr = [v["frac_of_8TBs"] for v in points.values()]
+        rows["sweep_points_bf16_sum_P2_P16_64_256MiB"] = {
+            "points": points, "min_frac_of_8TBs": min(fr),
+            "points_at_or_above_0.80": sum(f >= 0.8 for f in fr), "n_points": len(fr),
+            "outputs": "per-rank", "inputs": "uniform [-1, 1) bf16, seed 4, drawn on the device"}
+
+    # Buffers off a 16-byte boundary.  The configured RS(avg) + AG step on
+    # bf16 views that all start 2 bytes past a boundary (every buffer shares
+    # the offset: the vector kernels run from each buffer's first boundary),
+    # against the same step on aligned buffers; and an AllGather whose shards
+    # start 2 bytes past a boundary while the outputs are aligned (sources and
+    # destinations at different offsets: the shifting copy).
+    if want("misaligned"):
+        P, R, C = P_RANKS, ROWS, COLS
+        gen = torch.Generator(device=dev).manual_seed(1)
+        m = R // P * C
+
+        def views(nelem, off_bytes, k):
+            base = [torch.empty(nelem + 16, dtype=torch.bfloat16, device=dev) for _ in range(k)]
+            return base, [b_[off_bytes // 2:off_bytes // 2 + nelem] for b_ in base]
+
+        res = {}
+        for name, off in (("aligned", 0), ("views_2B_past_boundary", 2)):
+            _, xs = views(R * C, off, P)
+            for x in xs:
+                x.copy_(torch.randn(R * C, generator=gen, device=dev).to(torch.bfloat16))
+            _, rs = views(m, off, P)
+            _, ag = views(R * C, off, P)
+            g = dt.dt_group_create(P, dev.index)
+
+            def step():
+                dt.dt_barrier(g)
+                dt.dt_reduce_scatter(g, ALL, xs, rs, m, "bf16", "avg")
+                dt.dt_barrier(g)
+                dt.dt_all_gather(g, ALL, rs, ag, None, R // P, C * 2)
+
+            ms = time_events(step, 20, reps=STEADY_REPS)
+            ok = dt.dt_group_check(g) == dt.DT_OK
+            dt.dt_group_destroy(g)
+            res[name] = (ms, ok)
+            del xs, rs, ag
+        rs_b, ag_b = step_bytes()
+        ms0, ms1 = res["aligned"][0], res["views_2B_past_boundary"][0]
+        rows["rs_ag_step_bf16_P4_views_2B_past_boundary"] = {
+            "GB/s": round((rs_b + ag_b) / (ms1 * 1e-3) / 1e9, 1), "us": round(ms1 * 1e3, 2),
+            "aligned_us": round(ms0 * 1e3, 2), "ratio_to_aligned": round(ms0 / ms1, 4),
+            "status_ok": res["aligned"][1] and res["views_2B_past_boundary"][1]}
+        # the shifting copy: shards 2 bytes past a boundary, aligned outputs
+        n = 32 << 20                              # 64 MiB of bf16 per shard
+        g = dt.dt_group_create(P, dev.index)
+        res = {}
+        for name, off in (("aligned", 0), ("shards_2B_past_boundary", 2)):
+            _, sh = views(n, off, P)
+            for x in sh:
+                x.copy_(torch.rand(n, generator=gen, device=dev).to(torch.bfloat16))
+            ag = [torch.empty(P * n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+            res[name] = time_events(lambda: dt.dt_all_gather(g, ALL, sh, ag, None, 1, n * 2), 10,
+                                    reps=STEADY_REPS)
+            del sh, ag
+        ok = dt.dt_group_check(g) == dt.DT_OK
+        dt.dt_group_destroy(g)
+        b = (P + P * P) * n * 2
+        ms0, ms1 = res["aligned"], res["shards_2B_past_boundary"]
+        rows["all_gather_bf16_P4_64MiB_shards_2B_past_boundary"] = {
+            "GB/s": round(b / (ms1 * 1e-3) / 1e9, 1), "us": round(ms1 * 1e3, 2),
+            "aligned_us": round(ms0 * 1e3, 2), "ratio_to_aligned": round(ms0 / ms1, 4),
+            "status_ok": ok}
 
     torch.cuda.empty_cache()
     return rows

@@ -177,7 +177,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                 scalar_from = ve * EPV;   // ragged end of the tensor, if it is in this slice
             }
             for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kBucketThreads)
-                reduce_elem<DT, OP>(sp, 0, i, P, sp, P, p.avg_scale, p.avg_pow2);
+                reduce_elem<DT, OP>(sp, 0, (int64_t)i, P, sp, P, p.avg_scale, p.avg_pow2);
         }
         if (++t >= p.ntensors) break;
         bt = p.tensors[t];

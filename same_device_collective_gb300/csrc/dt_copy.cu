@@ -14,8 +14,11 @@
 // ranks receive it and no register or load/store-unit traffic is spent on the
 // bytes.  Destinations are written once and not read back here, so the
 // stores carry an evict-first L2 policy: their dirty lines leave L2 early
-// instead of being written back during the next kernel.  Anything else takes
-// a byte-wise kernel with the same tiling.
+// instead of being written back during the next kernel.  Segments whose
+// source and destinations share their offset past a 16-byte boundary (views
+// that start mid-vector) take the same kernels for their aligned middle and
+// copy their few edge bytes alongside; any other layout takes a kernel that
+// aligns every store and funnel-shifts the source into place.
 #include <atomic>
 
 #include "dt_internal.h"
@@ -34,6 +37,30 @@ __device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
         else hi = mid - 1;
     }
     return lo;
+}
+
+// The head and tail bytes of the launch's segments (see CopySeg), byte by
+// byte, in a small launch of their own next to the one that moves the
+// segments' aligned middles (folding them into those kernels, on the bulk
+// copy's idle lanes, slowed the aligned copies down: the 8-rank AllToAll of
+// 512 MiB per rank lost 23%).  Block b takes
+// segments b, b + gridDim.x, ...; its threads share each segment's edge bytes
+// and destinations.
+template <int NSEG, int NOUT>
+__global__ void __launch_bounds__(kThreads)
+copy_edge_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
+{
+    pdl_begin();
+    for (int s = blockIdx.x; s < p.nseg; s += gridDim.x) {
+        const CopySeg &sg = p.seg[s];
+        const uint32_t h = sg.head, e = (uint32_t)sg.head + sg.tail;
+        if (e == 0) continue;
+        for (uint32_t i = threadIdx.x; i < e * (uint32_t)sg.dst_count; i += kThreads) {
+            const uint32_t k = i / e, b = i - k * e;
+            const int64_t off = b < h ? (int64_t)b - (int64_t)h : (int64_t)(sg.bytes + (b - h));
+            static_cast<unsigned char *>(p.out[sg.dst_first + k])[(int64_t)sg.dst_off + off] = sg.src[off];
+        }
+    }
 }
 
 // Bulk-copy (TMA) kernel for 16-byte-aligned segments.  One thread per block
@@ -173,20 +200,95 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     bulk_wait_all();
 }
 
-// Any alignment: byte by byte, same tiling.
+// Any alignment: each (segment, destination) pair is copied on its own, in
+// tiles of kShiftChunks 16-byte chunks of the destination.  The destination's
+// bytes up to its first 16-byte boundary and after its last one go byte by
+// byte; in between, every chunk is one aligned 16-byte store.  Its source
+// bytes start `sh` bytes into an aligned source vector and end in the next
+// one: lane L of a warp loads aligned source vector c (c its chunk), takes
+// vector c + 1 from lane L + 1 (lane 31 loads it), and funnel-shifts the pair
+// by sh bytes.  Each aligned vector is loaded once per destination.  The first
+// and last vectors read may hold bytes just outside the source range (never
+// more than the rest of the 16-byte block that holds a source byte); those
+// bytes are discarded.
+constexpr uint64_t kShiftChunks = 512;                 // 8 KiB of destination per tile
+constexpr uint64_t kShiftTile = kShiftChunks * 16;
+
+__device__ __forceinline__ uint4 shift_pair(const uint4 &a, const uint4 &b, uint32_t sh)
+{
+    // bytes [sh, sh + 16) of the 32-byte little-endian sequence a, b
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t bits = (sh & 3) * 8;
+    uint32_t o[4];
+    switch (sh >> 2) {
+#define DT_SHIFT_CASE(q)                                                                  \
+    case q:                                                                               \
+        o[0] = __funnelshift_r(w[q + 0], w[q + 1], bits);                                 \
+        o[1] = __funnelshift_r(w[q + 1], w[q + 2], bits);                                 \
+        o[2] = __funnelshift_r(w[q + 2], w[q + 3], bits);                                 \
+        o[3] = __funnelshift_r(w[q + 3], w[q + 4], bits);                                 \
+        break;
+        DT_SHIFT_CASE(0)
+        DT_SHIFT_CASE(1)
+        DT_SHIFT_CASE(2)
+        DT_SHIFT_CASE(3)
+#undef DT_SHIFT_CASE
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 shfl_down_uint4(const uint4 &v)
+{
+    return make_uint4(__shfl_down_sync(0xFFFFFFFFu, v.x, 1), __shfl_down_sync(0xFFFFFFFFu, v.y, 1),
+                      __shfl_down_sync(0xFFFFFFFFu, v.z, 1), __shfl_down_sync(0xFFFFFFFFu, v.w, 1));
+}
+
+// Tiles of one (segment, destination) pair: enough for its bytes, at least one.
+__host__ __device__ __forceinline__ uint64_t shift_tiles(uint64_t bytes)
+{
+    const uint64_t t = (bytes + kShiftTile - 1) / kShiftTile;
+    return t ? t : 1;
+}
+
 template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kThreads)
-copy_byte_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
+copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
     pdl_begin();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         const CopySeg &sg = p.seg[find_seg(p, tile)];
-        const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
-        const uint64_t nb = sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes;
-        for (uint64_t b = threadIdx.x; b < nb; b += kThreads) {
-            const unsigned char c = sg.src[t0 + b];
-            for (int k = 0; k < sg.dst_count; ++k)
-                static_cast<unsigned char *>(p.out[sg.dst_first + k])[sg.dst_off + t0 + b] = c;
+        const uint64_t tpp = shift_tiles(sg.bytes);
+        const uint64_t idx = tile - sg.tile_begin;
+        const uint64_t k = idx / tpp, t = idx - k * tpp;
+        unsigned char *D = static_cast<unsigned char *>(p.out[sg.dst_first + (int)k]) + sg.dst_off;
+        const unsigned char *S = sg.src;
+        const uint64_t n = sg.bytes;
+        uint64_t dh = (16 - (reinterpret_cast<uintptr_t>(D) & 15)) & 15;   // bytes before the boundary
+        if (dh > n) dh = n;
+        const uint64_t nch = (n - dh) / 16;
+        if (t == 0)
+            for (uint64_t b = threadIdx.x; b < dh; b += kThreads) D[b] = S[b];
+        if (t == tpp - 1)
+            for (uint64_t b = dh + nch * 16 + threadIdx.x; b < n; b += kThreads) D[b] = S[b];
+        const uint64_t c0 = t * kShiftChunks;
+        const uint64_t c1 = c0 + kShiftChunks < nch ? c0 + kShiftChunks : nch;
+        if (c0 >= c1) continue;
+        const unsigned char *sp = S + dh;                  // source of chunk 0
+        const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(sp) & 15);
+        const uint4 *A = reinterpret_cast<const uint4 *>(sp - sh);    // aligned source vectors
+        uint4 *Dv = reinterpret_cast<uint4 *>(D + dh);
+        // warp w takes chunks [base, base + 32); the loop bound is the same
+        // for every lane, so the whole warp reaches each shuffle
+        for (uint64_t base = c0 + (uint64_t)warp * 32; base < c1; base += kThreads) {
+            const uint64_t c = base + lane;
+            // vector c is read for chunk c (c < c1) and, when sh > 0, for
+            // chunk c - 1 (c <= c1): both hold bytes of the source
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (c < c1 || (sh && c == c1)) w = __ldcs(A + c);
+            uint4 nx = shfl_down_uint4(w);
+            if (lane == 31 && sh && c < c1) nx = __ldcs(A + c + 1);
+            if (c < c1) __stcs(Dv + c, sh ? shift_pair(w, nx, sh) : w);
         }
     }
 }
@@ -289,20 +391,66 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
     int used = 0;
     for (int i = 0; i < nseg; ++i) {
         if (segs[i].bytes == 0 || segs[i].dst_count == 0) continue;
-        p.seg[used++] = segs[i];
+        p.seg[used] = segs[i];
+        p.seg[used].head = p.seg[used].tail = 0;
+        ++used;
         if (segs[i].dst_count > max_dst) max_dst = segs[i].dst_count;
     }
     if (used == 0) return cudaSuccess;   // nothing to move
     p.nseg = used;
 
     if (!vec) {
-        const uint64_t tiles = cut_tiles(p, 4096);
-        void (*fn)(CopyParams<NSEG, NOUT>) = copy_byte_kernel<NSEG, NOUT>;
-        int resident = 0;
-        cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
+        // Does every segment's source lie as far past a 16-byte boundary as
+        // each of its destinations?  Then the aligned middle of every segment
+        // takes the fast paths below and the edges go byte by byte.
+        bool same = true;
+        for (int i = 0; i < p.nseg && same; ++i) {
+            const CopySeg &sg = p.seg[i];
+            const uintptr_t m = reinterpret_cast<uintptr_t>(sg.src) & 15;
+            for (int k = 0; k < sg.dst_count && same; ++k)
+                same = ((reinterpret_cast<uintptr_t>(p.out[sg.dst_first + k]) + sg.dst_off) & 15) == m;
+        }
+        if (!same) {
+            // otherwise every (segment, destination) pair is shifted on its own
+            uint64_t tiles = 0;
+            for (int i = 0; i < p.nseg; ++i) {
+                p.seg[i].tile_begin = tiles;
+                tiles += shift_tiles(p.seg[i].bytes) * (uint64_t)p.seg[i].dst_count;
+            }
+            p.total_tiles = tiles;
+            p.tile_bytes = kShiftTile;
+            void (*fn)(CopyParams<NSEG, NOUT>) = copy_shift_kernel<NSEG, NOUT>;
+            int resident = 0;
+            cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
+            if (e != cudaSuccess) return e;
+            const uint64_t cap = (uint64_t)resident * 4;
+            const uint64_t gx = tiles < cap ? tiles : cap;
+            return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
+        }
+        for (int i = 0; i < p.nseg; ++i) {
+            CopySeg &sg = p.seg[i];
+            uint64_t h = (16 - (reinterpret_cast<uintptr_t>(sg.src) & 15)) & 15;
+            if (h > sg.bytes) h = sg.bytes;
+            const uint64_t body = (sg.bytes - h) & ~(uint64_t)15;
+            sg.head = (uint8_t)h;
+            sg.tail = (uint8_t)(sg.bytes - h - body);
+            sg.src += h;
+            sg.dst_off += h;
+            sg.bytes = body;
+        }
+        const uint64_t gx = (uint64_t)p.nseg;
+        cudaError_t e = launch_kernel(copy_edge_kernel<NSEG, NOUT>, dim3((unsigned)gx), dim3(kThreads), 0,
+                                      s, false, p);
         if (e != cudaSuccess) return e;
-        const uint64_t gx = tiles < (uint64_t)resident ? tiles : (uint64_t)resident;
-        return launch_kernel(fn, dim3((unsigned)gx), dim3(kThreads), 0, s, false, p);
+        // the middles: drop segments that are edges only
+        int kept = 0;
+        for (int i = 0; i < p.nseg; ++i)
+            if (p.seg[i].bytes) p.seg[kept++] = p.seg[i];
+        if (kept == 0) return cudaSuccess;
+        p.nseg = kept;
+        max_dst = 0;
+        for (int i = 0; i < p.nseg; ++i)
+            if (p.seg[i].dst_count > max_dst) max_dst = p.seg[i].dst_count;
     }
     uint64_t src_bytes = 0;
     for (int i = 0; i < p.nseg; ++i) src_bytes += p.seg[i].bytes;

@@ -678,16 +678,21 @@ dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *cons
 
     dt::ReduceParams p;
     memset(&p, 0, sizeof p);
-    bool vec = true;
-    for (int r = 0; r < P; ++r) {
-        p.in[r] = in[r];
-        vec = vec && aligned16(in[r]);
-    }
-    for (int q = 0; q < nout; ++q) {
-        p.out[q] = out[q];
-        vec = vec && aligned16(out[q]);
-    }
-    p.n = count;
+    // The vector kernel runs when every buffer lies the same whole number of
+    // elements past a 16-byte boundary (aligned buffers, or views that share
+    // an offset): it gets the buffers from that boundary on, and reduces the
+    // head elements before it on the element path.
+    const size_t es = elem_bytes(dtype);
+    const uintptr_t mis = (uintptr_t)in[0] & 15;
+    const size_t head = ((16 - mis) & 15) / es;
+    bool vec = mis % es == 0 && head < count;
+    for (int r = 0; r < P; ++r) vec = vec && ((uintptr_t)in[r] & 15) == mis;
+    for (int q = 0; q < nout; ++q) vec = vec && ((uintptr_t)out[q] & 15) == mis;
+    const size_t skip = vec ? head * es : 0;
+    for (int r = 0; r < P; ++r) p.in[r] = static_cast<const unsigned char *>(in[r]) + skip;
+    for (int q = 0; q < nout; ++q) p.out[q] = static_cast<unsigned char *>(out[q]) + skip;
+    p.head = vec ? (uint32_t)head : 0;
+    p.n = count - p.head;
     p.job_stride = 0;
     p.P = P;
     p.out_per_job = nout;
@@ -736,14 +741,23 @@ dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void 
 
     dt::ReduceParams p;
     memset(&p, 0, sizeof p);
-    const size_t epv = 16 / es;
-    bool vec = recv_count % epv == 0;
+    // Job (shard) j reads every input at element j * recv_count and writes
+    // out[j].  The vector kernel runs when shards are whole 16-byte vectors
+    // and every input and output lies the same whole number of elements past
+    // a 16-byte boundary: it gets the buffers from that boundary on, and
+    // reduces each shard's head elements before it on the element path.
+    const uintptr_t mis = (uintptr_t)in[0] & 15;
+    const size_t head = ((16 - mis) & 15) / es;
+    bool vec = (recv_count * es) % 16 == 0 && mis % es == 0 && head < recv_count;
+    for (int r = 0; r < P; ++r)
+        vec = vec && ((uintptr_t)in[r] & 15) == mis && ((uintptr_t)out[r] & 15) == mis;
+    const size_t skip = vec ? head * es : 0;
     for (int r = 0; r < P; ++r) {
-        p.in[r] = in[r];
-        p.out[r] = out[r];
-        vec = vec && aligned16(in[r]) && aligned16(out[r]);
+        p.in[r] = static_cast<const unsigned char *>(in[r]) + skip;
+        p.out[r] = static_cast<unsigned char *>(out[r]) + skip;
     }
-    p.n = recv_count;
+    p.head = vec ? (uint32_t)head : 0;
+    p.n = recv_count - p.head;
     p.job_stride = recv_count;
     p.P = P;
     p.out_per_job = 1;
@@ -803,7 +817,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
         }
     }
 
-    dt::CopySeg segs[DT_MAX_RANKS];
+    dt::CopySeg segs[DT_MAX_RANKS] = {};
     bool vec = true;
     for (int r = 0; r < P; ++r) {
         segs[r].src = static_cast<const unsigned char *>(in[r]);
@@ -811,7 +825,7 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
         segs[r].dst_off = off[r] * row_bytes;
         segs[r].tile_begin = 0;
         segs[r].dst_first = 0;
-        segs[r].dst_count = nout;
+        segs[r].dst_count = (int16_t)nout;
         if (segs[r].bytes)
             vec = vec && aligned16(in[r]) && segs[r].bytes % 16 == 0 && segs[r].dst_off % 16 == 0;
     }
@@ -870,7 +884,7 @@ dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *con
             sg.bytes = chunk_bytes;
             sg.dst_off = (size_t)i * chunk_bytes;
             sg.tile_begin = 0;
-            sg.dst_first = j;
+            sg.dst_first = (int16_t)j;
             sg.dst_count = 1;
         }
     }
@@ -1105,7 +1119,7 @@ dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, v
             if (overlaps(o, o2)) return DT_ERR_INVALID;
         }
     }
-    dt::CopySeg segs[DT_MAX_RANKS];
+    dt::CopySeg segs[DT_MAX_RANKS] = {};
     void *outs[DT_MAX_RANKS] = {};
     bool vec = block % 16 == 0;
     for (int r = 0; r < P; ++r) {
@@ -1113,7 +1127,7 @@ dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, v
         segs[r].bytes = block;
         segs[r].dst_off = 0;
         segs[r].tile_begin = 0;
-        segs[r].dst_first = r;
+        segs[r].dst_first = (int16_t)r;
         segs[r].dst_count = 1;
         outs[r] = out[r];
         vec = vec && aligned16(in[r]) && aligned16(out[r]);
@@ -1171,7 +1185,7 @@ dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, 
 
     // segment r: rank r's shard to out[q * P + r] for every q; the table is
     // stored by source (outs[r * P + q]) so a segment's destinations are adjacent
-    dt::CopySeg segs[DT_MAX_RANKS];
+    dt::CopySeg segs[DT_MAX_RANKS] = {};
     std::vector<void *> outs((size_t)P * P);
     bool vec = true;
     for (int r = 0; r < P; ++r) {
@@ -1179,8 +1193,8 @@ dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, 
         segs[r].bytes = nb[r];
         segs[r].dst_off = 0;
         segs[r].tile_begin = 0;
-        segs[r].dst_first = r * P;
-        segs[r].dst_count = P;
+        segs[r].dst_first = (int16_t)(r * P);
+        segs[r].dst_count = (int16_t)P;
         if (nb[r]) vec = vec && aligned16(in[r]) && nb[r] % 16 == 0;
         for (int q = 0; q < P; ++q) {
             outs[(size_t)r * P + q] = out[q * P + r];

@@ -37,7 +37,11 @@ struct ErrorSink {
 // Job j (blockIdx.y) reduces elements [j * job_stride, j * job_stride + n)
 // of every input and writes them to out[j * out_per_job + k], k < out_per_job.
 // AllReduce: 1 job, out_per_job = P (or 1 shared).  ReduceScatter: P jobs,
-// out_per_job = 1, job_stride = n.
+// out_per_job = 1, job_stride = n.  The vector kernel takes 16-byte-aligned
+// pointers.  Buffers that all lie the same whole number of elements past a
+// 16-byte boundary reach it advanced by `head` elements to that boundary
+// (and n reduced by head); the kernel then reduces the head elements before
+// each job's start on the element path, at negative indices.
 struct ReduceParams {
     const void *in[DT_MAX_RANKS];
     void *out[DT_MAX_RANKS];
@@ -47,20 +51,34 @@ struct ReduceParams {
     int32_t avg_pow2;    // 1: multiply by avg_scale (same rounding as /P); 0: divide by P
     int32_t P;
     int32_t out_per_job;
+    uint32_t head;       // elements before the pointers above, 0..15
+    uint32_t pad;
 };
 
 // ---- byte copies (AllGather, AllToAll) ------------------------------------
 // Segment s copies `bytes` from src to out[dst_first + k] + dst_off for
 // k < dst_count; segments are cut into tiles of tile_bytes and tile t of the
 // launch belongs to the segment with tile_begin <= t < next tile_begin.
+// Callers leave head and tail at 0.  When a segment's source and
+// destinations lie the same distance past a 16-byte boundary, the launcher
+// moves the bytes before the source's first boundary and after its last one
+// into head and tail: the segment then covers [src - head, src + bytes +
+// tail), its 16-byte-aligned middle [src, src + bytes) goes through the
+// vector or bulk-copy kernels, and the edges byte by byte.
 struct CopySeg {
     const unsigned char *src;
     uint64_t bytes;
     uint64_t dst_off;
     uint64_t tile_begin;
-    int32_t dst_first;
-    int32_t dst_count;
+    int16_t dst_first;    // < DT_MAX_RANKS^2
+    int16_t dst_count;    // <= DT_MAX_RANKS^2
+    uint8_t head;         // < 16
+    uint8_t tail;         // < 16
+    uint16_t pad;
 };
+// 40 bytes: an AllToAll's 256 entries take 10 KiB of the kernel's parameter
+// block.
+static_assert(sizeof(CopySeg) == 40, "segment entries stay 40 bytes");
 
 template <int NSEG, int NOUT = DT_MAX_RANKS>
 struct CopyParams {

@@ -187,13 +187,14 @@ __device__ __forceinline__ uint4 reduce_vec16(const uint4 (&x)[PMAX], int P, flo
 
 // Element-wise form: reduce element in_off + i of each rank buffer base[r]
 // and store it as element i of dst[k], k < ndst.  Used for ragged tails and
-// unaligned buffers.
+// unaligned buffers, and (with i < 0) for the elements just before buffers
+// that the vector kernel was handed from their first 16-byte boundary on.
 template <int DT, int OP>
-__device__ __forceinline__ void reduce_elem(const void *const *base, uint64_t in_off, uint64_t i,
+__device__ __forceinline__ void reduce_elem(const void *const *base, int64_t in_off, int64_t i,
                                             int P, void *const *dst, int ndst, float scale,
                                             int pow2)
 {
-    const uint64_t j = in_off + i;
+    const int64_t j = in_off + i;
     if constexpr (DT == DT_I32) {
         int32_t acc = static_cast<const int32_t *>(base[0])[j];
         for (int r = 1; r < P; ++r) acc = pick_i<OP>(acc, static_cast<const int32_t *>(base[r])[j]);

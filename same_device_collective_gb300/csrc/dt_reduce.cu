@@ -70,11 +70,15 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
         }
     }
 
-    // ragged tail: the last n % EPV elements of the job, element by element
+    // ragged tail: the last n % EPV elements of the job, element by element,
+    // and the head elements before the job's first vector
     if (blockIdx.x == 0) {
-        const uint64_t in_elem_off = (uint64_t)j * p.job_stride;
+        const int64_t in_elem_off = (int64_t)j * (int64_t)p.job_stride;
         for (uint64_t i = nvec * EPV + threadIdx.x; i < p.n; i += kThreads)
-            reduce_elem<DT, OP>(p.in, in_elem_off, i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+        if (threadIdx.x < p.head)
+            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)threadIdx.x - (int64_t)p.head, P, dst, ndst,
+                                p.avg_scale, p.avg_pow2);
     }
 }
 
@@ -85,11 +89,12 @@ reduce_scalar_kernel(const __grid_constant__ ReduceParams p)
 {
     pdl_begin();
     const int j = blockIdx.y;
-    const uint64_t in_elem_off = (uint64_t)j * p.job_stride;
+    const int64_t in_elem_off = (int64_t)j * (int64_t)p.job_stride;
     void *const *dst = p.out + j * p.out_per_job;
     for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n;
          i += (uint64_t)gridDim.x * kThreads)
-        reduce_elem<DT, OP>(p.in, in_elem_off, i, p.P, dst, p.out_per_job, p.avg_scale, p.avg_pow2);
+        reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, p.P, dst, p.out_per_job, p.avg_scale,
+                            p.avg_pow2);
 }
 
 using ReduceFn = void (*)(ReduceParams);
