@@ -200,17 +200,18 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     bulk_wait_all();
 }
 
-// Any alignment: each (segment, destination) pair is copied on its own, in
-// tiles of kShiftChunks 16-byte chunks of the destination.  The destination's
-// bytes up to its first 16-byte boundary and after its last one go byte by
-// byte; in between, every chunk is one aligned 16-byte store.  Its source
-// bytes start `sh` bytes into an aligned source vector and end in the next
-// one: lane L of a warp loads aligned source vector c (c its chunk), takes
-// vector c + 1 from lane L + 1 (lane 31 loads it), and funnel-shifts the pair
-// by sh bytes.  Each aligned vector is loaded once per destination.  The first
-// and last vectors read may hold bytes just outside the source range (never
-// more than the rest of the 16-byte block that holds a source byte); those
-// bytes are discarded.
+// Any alignment: the destination is cut into tiles of kShiftChunks 16-byte
+// chunks.  Its bytes up to its first 16-byte boundary and after its last one
+// go byte by byte; in between, every chunk is one aligned 16-byte store.  The
+// chunk's source bytes start `sh` bytes into an aligned source vector and end
+// in the next one: lane L of a warp loads aligned source vector c (c its
+// chunk), takes vector c + 1 from lane L + 1 (lane 31 loads it), and
+// funnel-shifts the pair by sh bytes.  A segment whose destinations share
+// their offset past a boundary is shifted once and stored to each of them;
+// otherwise each destination takes its own pass.  The first and last vectors
+// read may hold bytes just outside the source range (never more than the
+// rest of the 16-byte block that holds a source byte); those bytes are
+// discarded.
 constexpr uint64_t kShiftChunks = 512;                 // 8 KiB of destination per tile
 constexpr uint64_t kShiftTile = kShiftChunks * 16;
 
@@ -260,24 +261,29 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         const CopySeg &sg = p.seg[find_seg(p, tile)];
         const uint64_t tpp = shift_tiles(sg.bytes);
         const uint64_t idx = tile - sg.tile_begin;
-        const uint64_t k = idx / tpp, t = idx - k * tpp;
-        unsigned char *D = static_cast<unsigned char *>(p.out[sg.dst_first + (int)k]) + sg.dst_off;
+        // one pass for all destinations, or tiles of one destination at a time
+        const int k0 = sg.one_pass ? 0 : (int)(idx / tpp);
+        const int nk = sg.one_pass ? sg.dst_count : 1;
+        const uint64_t t = sg.one_pass ? idx : idx - (uint64_t)k0 * tpp;
+        unsigned char *const *outs = reinterpret_cast<unsigned char *const *>(p.out) + sg.dst_first + k0;
         const unsigned char *S = sg.src;
         const uint64_t n = sg.bytes;
-        uint64_t dh = (16 - (reinterpret_cast<uintptr_t>(D) & 15)) & 15;   // bytes before the boundary
-        if (dh > n) dh = n;
+        uint64_t dh = (16 - ((reinterpret_cast<uintptr_t>(outs[0]) + sg.dst_off) & 15)) & 15;
+        if (dh > n) dh = n;                                // bytes before the boundary
         const uint64_t nch = (n - dh) / 16;
-        if (t == 0)
-            for (uint64_t b = threadIdx.x; b < dh; b += kThreads) D[b] = S[b];
-        if (t == tpp - 1)
-            for (uint64_t b = dh + nch * 16 + threadIdx.x; b < n; b += kThreads) D[b] = S[b];
+        for (int k = 0; k < nk; ++k) {
+            unsigned char *D = outs[k] + sg.dst_off;
+            if (t == 0)
+                for (uint64_t b = threadIdx.x; b < dh; b += kThreads) D[b] = S[b];
+            if (t == tpp - 1)
+                for (uint64_t b = dh + nch * 16 + threadIdx.x; b < n; b += kThreads) D[b] = S[b];
+        }
         const uint64_t c0 = t * kShiftChunks;
         const uint64_t c1 = c0 + kShiftChunks < nch ? c0 + kShiftChunks : nch;
         if (c0 >= c1) continue;
         const unsigned char *sp = S + dh;                  // source of chunk 0
         const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(sp) & 15);
         const uint4 *A = reinterpret_cast<const uint4 *>(sp - sh);    // aligned source vectors
-        uint4 *Dv = reinterpret_cast<uint4 *>(D + dh);
         // warp w takes chunks [base, base + 32); the loop bound is the same
         // for every lane, so the whole warp reaches each shuffle
         for (uint64_t base = c0 + (uint64_t)warp * 32; base < c1; base += kThreads) {
@@ -288,7 +294,11 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
             if (c < c1 || (sh && c == c1)) w = __ldcs(A + c);
             uint4 nx = shfl_down_uint4(w);
             if (lane == 31 && sh && c < c1) nx = __ldcs(A + c + 1);
-            if (c < c1) __stcs(Dv + c, sh ? shift_pair(w, nx, sh) : w);
+            if (c < c1) {
+                const uint4 v = sh ? shift_pair(w, nx, sh) : w;
+                for (int k = 0; k < nk; ++k)
+                    __stcs(reinterpret_cast<uint4 *>(outs[k] + sg.dst_off + dh) + c, v);
+            }
         }
     }
 }
@@ -411,11 +421,19 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
                 same = ((reinterpret_cast<uintptr_t>(p.out[sg.dst_first + k]) + sg.dst_off) & 15) == m;
         }
         if (!same) {
-            // otherwise every (segment, destination) pair is shifted on its own
+            // otherwise the source is shifted into place: once for all of a
+            // segment's destinations when they share their offset past a
+            // boundary, else once per destination
             uint64_t tiles = 0;
             for (int i = 0; i < p.nseg; ++i) {
-                p.seg[i].tile_begin = tiles;
-                tiles += shift_tiles(p.seg[i].bytes) * (uint64_t)p.seg[i].dst_count;
+                CopySeg &sg = p.seg[i];
+                const uintptr_t m0 = (reinterpret_cast<uintptr_t>(p.out[sg.dst_first]) + sg.dst_off) & 15;
+                bool one = true;
+                for (int k = 1; k < sg.dst_count && one; ++k)
+                    one = ((reinterpret_cast<uintptr_t>(p.out[sg.dst_first + k]) + sg.dst_off) & 15) == m0;
+                sg.one_pass = one ? 1 : 0;
+                sg.tile_begin = tiles;
+                tiles += shift_tiles(sg.bytes) * (one ? 1 : (uint64_t)sg.dst_count);
             }
             p.total_tiles = tiles;
             p.tile_bytes = kShiftTile;

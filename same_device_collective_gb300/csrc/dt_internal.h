@@ -74,7 +74,8 @@ struct CopySeg {
     int16_t dst_count;    // <= DT_MAX_RANKS^2
     uint8_t head;         // < 16
     uint8_t tail;         // < 16
-    uint16_t pad;
+    uint16_t one_pass;    // shifting copy: the destinations share their offset past a
+                          // 16-byte boundary, so one pass over the source serves them all
 };
 // 40 bytes: an AllToAll's 256 entries take 10 KiB of the kernel's parameter
 // block.

@@ -116,8 +116,9 @@ def test_allreduce_shared_offset_in_place(dt, dtype):
 @pytest.mark.parametrize("P", [2, 3, 8])
 def test_reduce_scatter_shard_offsets(dt, dtype, op, m, elems_off, P):
     # inputs share an offset; out[j] sits where shard j of the inputs sits
-    # relative to a 16-byte boundary, so every job takes the vector kernel
-    # with its own count of leading elements (m odd: they differ per job)
+    # relative to a 16-byte boundary.  Shards of whole 16-byte vectors then
+    # take the vector kernel from the first boundary; the others (m odd: the
+    # shards' offsets differ) the element path.
     es = ELEM[dtype]
     xs = rand_inputs(P, P * m, dtype, 31 * m + P)
     snap = [host(x).copy() for x in xs]
@@ -134,11 +135,14 @@ def test_reduce_scatter_shard_offsets(dt, dtype, op, m, elems_off, P):
 
 
 # ----------------------------------------------------------------- copies
-@pytest.mark.parametrize("layout", ["shared_offset", "mixed"])
+@pytest.mark.parametrize("layout", ["shared_offset", "mixed", "outputs_apart"])
 @pytest.mark.parametrize("row_bytes", [8192, 16, 12, 7, 8190])
 @pytest.mark.parametrize("P", [2, 4, 16])
 @pytest.mark.parametrize("shared", [False, True])
 def test_all_gather_offsets(dt, layout, row_bytes, P, shared):
+    # shared_offset: shards and outputs 2 bytes past a boundary; mixed:
+    # shards 2 bytes past, outputs aligned; outputs_apart: every output at
+    # its own offset (each destination shifted on its own pass)
     rng = np.random.default_rng(row_bytes + P)
     rows = [int(r) for r in rng.integers(0, 300, P)]
     rows[0] = max(rows[0], 1)
@@ -149,7 +153,8 @@ def test_all_gather_offsets(dt, layout, row_bytes, P, shared):
     out_shift = in_shift if layout == "shared_offset" else 0
     ins = [placed(x, in_shift) for x in shards]
     nout = 1 if shared else P
-    outs = [empty_at(total, torch.uint8, out_shift) for _ in range(nout)]
+    outs = [empty_at(total, torch.uint8, (out_shift + 3 * q) % 16 if layout == "outputs_apart" else out_shift)
+            for q in range(nout)]
     out_views = [outs[0][1]] * P if shared else [v for _, v in outs]
     with group(P) as g:
         dt.dt_all_gather(g, dt.DT_ALL_RANKS, [v for _, v in ins], out_views, rows, 0, row_bytes,
