@@ -891,6 +891,13 @@ NCU_CASES = {
     "uneven_all_gather": ("copy_bulk_kernel", 2,
                           "uneven AllGather int32, P=8, rows U[1, 2048] x 4096, per-rank outputs"),
     "barrier": ("barrier_kernel", 2, "signal-window barrier, P=16"),
+    "allreduce_large": ("reduce_vec_kernel", 2, "AllReduce kSum f32, P=8, 64 MiB per rank"),
+    "all_to_all_2d": ("copy2d_kernel", 2, "AllToAll S(0) -> S(1) bf16, P=8, [8192, 4096] per rank"),
+    "small_gather": ("copy_vec_kernel", 2, "AllGather bf16, P=4, 256 KiB shards, per-rank outputs"),
+    "reduce_scalar": ("reduce_scalar_kernel", 2,
+                      "AllReduce kSum bf16, P=4, 16 MiB per rank, inputs at different offsets"),
+    "shift_gather": ("copy_shift_kernel", 2,
+                     "AllGather bf16, P=4, 16 MiB shards 2 bytes past a boundary, aligned outputs"),
 }
 
 
@@ -941,6 +948,36 @@ def run_ncu_case(name):
     elif name == "barrier":
         g = dt.dt_group_create(16, dev.index)
         call = lambda: dt.dt_barrier(g)
+    elif name == "allreduce_large":
+        gen = torch.Generator(device=dev).manual_seed(4)
+        n = 16 << 20
+        xs = [torch.rand(n, generator=gen, device=dev) for _ in range(8)]
+        outs = [torch.empty_like(x) for x in xs]
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "f32", "sum")
+    elif name == "all_to_all_2d":
+        w = workloads.all_to_all_tokens(rows=8192, device=str(dev))
+        R8, C8 = w.inputs[0].shape
+        outs = [torch.empty(8 * R8, C8 // 8, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_all_to_all_2d(g, ALL, w.inputs, outs, R8, C8, 2, 0, 1)
+    elif name in ("small_gather", "shift_gather"):
+        n = (128 << 10) if name == "small_gather" else (8 << 20)    # bf16 elements per shard
+        off = 0 if name == "small_gather" else 1
+        gen = torch.Generator(device=dev).manual_seed(4)
+        base = [torch.rand(n + 8, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
+        shards = [b_[off:off + n] for b_ in base]
+        outs = [torch.empty(4 * n, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        g = dt.dt_group_create(4, dev.index)
+        call = lambda: dt.dt_all_gather(g, ALL, shards, outs, None, 1, n * 2)
+    elif name == "reduce_scalar":
+        n = 8 << 20
+        gen = torch.Generator(device=dev).manual_seed(4)
+        base = [torch.rand(n + 8, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
+        xs = [b_[r:r + n] for r, b_ in enumerate(base)]          # offsets 0, 2, 4, 6 bytes
+        outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        g = dt.dt_group_create(4, dev.index)
+        call = lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "bf16", "sum")
     else:
         raise ValueError(name)
     for _ in range(5):
