@@ -557,6 +557,18 @@ def measure_rows(dt, dev, peak, only=None):
         except (OSError, ValueError, IndexError, subprocess.TimeoutExpired) as ex:
             native = {"error": f"{type(ex).__name__}: {ex}"}
         rows["rank_local_rs_ag_step_bf16_P4_native_threads"] = native
+        # the same with one stream shared by all rank threads: no cross-stream
+        # event waits, so the gap to the row above is what those waits cost
+        try:
+            res = subprocess.run([tool, str(P), str(R), str(C), "2000", "shared"], capture_output=True,
+                                 text=True, timeout=300)
+            shared = json.loads(res.stdout.strip().splitlines()[-1])
+            if "GB/s" in shared:
+                shared["frac_of_measured_hbm"] = round(shared["GB/s"] / peak, 4)
+            shared["caller"] = "C++ std::thread per rank (rank_local_step), one shared stream"
+        except (OSError, ValueError, IndexError, subprocess.TimeoutExpired) as ex:
+            shared = {"error": f"{type(ex).__name__}: {ex}"}
+        rows["rank_local_rs_ag_step_bf16_P4_native_threads_shared_stream"] = shared
 
     # Remaining placement conversions at the configured shapes: R -> S of a
     # replicated bf16 [8192, 4096] tensor (P=4), AllGatherIntoVec of its

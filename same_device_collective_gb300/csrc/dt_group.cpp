@@ -327,6 +327,7 @@ bool same_call(const dt_group::RankCall &a, const dt_group::RankCall &b)
 // The last rank of a round launches the group-wide call on its own stream,
 // after that stream has waited for every other rank's inputs (their ready
 // events: the DestGet / StreamWaitEvent step of the TensorStore protocol).
+// Ranks that passed the launching stream itself need no wait, either way.
 dt_status launch_round(dt_group *g, int last)
 {
     const int P = g->P;
@@ -335,7 +336,9 @@ dt_status launch_round(dt_group *g, int last)
         if (!same_call(g->rv_call[r], c0)) return DT_ERR_INVALID;
     cudaStream_t s = g->rv_call[last].stream;
     for (int r = 0; r < P; ++r)
-        if (r != last && cudaStreamWaitEvent(s, g->rv_ready[r], 0) != cudaSuccess) return DT_ERR_CUDA;
+        if (r != last && g->rv_call[r].stream != s &&
+            cudaStreamWaitEvent(s, g->rv_ready[r], 0) != cudaSuccess)
+            return DT_ERR_CUDA;
     const void *ins[DT_MAX_RANKS];
     void *outs[DT_MAX_RANKS];
     size_t rows[DT_MAX_RANKS];
@@ -431,8 +434,9 @@ dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
         if (g->rv_round != my_round) {
             dt_status st = g->rv_status[slot];
             cudaEvent_t done = g->rv_done[slot];
+            const bool same_stream = g->rv_launch[slot] == call.stream;
             lk.unlock();
-            if (st == DT_OK && cudaStreamWaitEvent(call.stream, done, 0) != cudaSuccess)
+            if (st == DT_OK && !same_stream && cudaStreamWaitEvent(call.stream, done, 0) != cudaSuccess)
                 st = DT_ERR_CUDA;
             return st;
         }
@@ -449,6 +453,7 @@ dt_status rank_local(dt_group *g, int rank, const dt_group::RankCall &call)
     dt_status st = launch_round(g, rank);
     if (st == DT_OK && cudaEventRecord(g->rv_done[slot], call.stream) != cudaSuccess) st = DT_ERR_CUDA;
     g->rv_status[slot] = st;
+    g->rv_launch[slot] = call.stream;
     for (int r = 0; r < DT_MAX_RANKS; ++r) g->rv_present[r] = false;
     g->rv_arrived = 0;
     ++g->rv_round;

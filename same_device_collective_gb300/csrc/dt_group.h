@@ -89,6 +89,7 @@ struct dt_group {
     dt_status rv_status[2] = {DT_OK, DT_OK};
     cudaEvent_t rv_ready[DT_MAX_RANKS] = {};
     cudaEvent_t rv_done[2] = {nullptr, nullptr};
+    cudaStream_t rv_launch[2] = {nullptr, nullptr};   // the stream round (parity) launched on
 
     // async scopes: the communication stream, the scope's start event and a
     // pool of work handles (each owns an end event)

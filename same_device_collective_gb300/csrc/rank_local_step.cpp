@@ -11,7 +11,11 @@
 // and the group's status.  No Python is involved, so the figure is the
 // library's own rank-local cost.
 //
-// Usage: rank_local_step [P rows cols steps]      (defaults 4 8192 4096 2000)
+// Usage: rank_local_step [P rows cols steps [shared]]   (defaults 4 8192 4096 2000)
+//
+// With "shared" every rank passes the same stream: the library then needs no
+// cross-stream event waits at all, so the difference between the two runs is
+// the cost of those waits.
 //
 // The inputs are filled with one constant: the step's memory traffic does not
 // depend on the values, and the results are not checked here (the tests do).
@@ -20,6 +24,7 @@
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
+#include <string>
 #include <thread>
 #include <vector>
 
@@ -41,6 +46,7 @@ int main(int argc, char **argv)
     const size_t rows = argc > 2 ? std::strtoull(argv[2], nullptr, 10) : 8192;
     const size_t cols = argc > 3 ? std::strtoull(argv[3], nullptr, 10) : 4096;
     const int steps = argc > 4 ? std::atoi(argv[4]) : 2000;
+    const bool shared = argc > 5 && std::string(argv[5]) == "shared";
     if (P < 1 || P > DT_MAX_RANKS || rows == 0 || cols == 0 || rows % P || steps < 1)
         return fail("arguments", "need 1 <= P <= 16, rows % P == 0, steps >= 1");
     const size_t shard_rows = rows / P;
@@ -68,7 +74,7 @@ int main(int argc, char **argv)
         for (int r = 0; r < P; ++r)
             threads.emplace_back([&, r] {
                 if (cudaSetDevice(0) != cudaSuccess) { bad[r] = DT_ERR_CUDA; return; }
-                void *s = streams[r];
+                void *s = streams[shared ? 0 : r];
                 for (int i = 0; i < k && !bad[r]; ++i) {
                     int e = dt_barrier(g, r, s);
                     if (!e) e = dt_reduce_scatter(g, r, &xs[r], &rs[r], shard_rows * cols, DT_BF16,
@@ -98,9 +104,10 @@ int main(int argc, char **argv)
     // ReduceScatter: P inputs read, P shards written; AllGather: P shards read, P outputs written
     const double bytes = (double)P * in_bytes + P * shard_bytes + P * shard_bytes + (double)P * in_bytes;
     std::printf("{\"P\": %d, \"rows\": %zu, \"cols\": %zu, \"steps\": %d, \"us_per_step\": %.2f, "
-                "\"host_issue_us_per_step\": %.2f, \"GB/s\": %.1f, \"status_ok\": %s}\n",
+                "\"host_issue_us_per_step\": %.2f, \"GB/s\": %.1f, \"streams\": \"%s\", "
+                "\"status_ok\": %s}\n",
                 P, rows, cols, steps, wall_us, host_us, bytes / (wall_us * 1e-6) / 1e9,
-                check == DT_OK ? "true" : "false");
+                shared ? "one shared by all ranks" : "one per rank", check == DT_OK ? "true" : "false");
 
     for (int r = 0; r < P; ++r) {
         cudaStreamDestroy(streams[r]);

@@ -193,20 +193,25 @@ def test_native_thread_driver_runs_the_rank_local_step():
     assert bad.returncode != 0 and "error" in json.loads(bad.stdout.strip().splitlines()[-1])
 
 
+@pytest.mark.parametrize("shared_stream", [False, True])
 @pytest.mark.parametrize("P", [3, 8])
-def test_rank_local_chained_rounds_stay_ordered(dt, P):
+def test_rank_local_chained_rounds_stay_ordered(dt, P, shared_stream):
     # P threads run the same seeded sequence of 120 rounds.  Each round first
     # updates the rank's buffer on its own stream (b = 0.5 b + (k + r)), then
     # makes one rank-local call on it: an in-place AllReduce, a ReduceScatter
     # (avg) followed by an AllGather back into b, an AllToAll copied back into
     # b, or a bare barrier.  Every input depends on the previous collective's
     # output, so an ordering slip anywhere shows in the final buffers, which a
-    # host replica built from the oracle must match bit for bit.
+    # host replica built from the oracle must match bit for bit.  With
+    # shared_stream every rank thread uses one stream (the calls then need no
+    # cross-stream waits).
     K, n = 120, 24_024
     m = n // P
     rng = np.random.default_rng(P)
     kinds = rng.choice(["ar", "rs_ag", "a2a", "barrier"], size=K, p=[0.35, 0.3, 0.2, 0.15])
     streams = [torch.cuda.Stream() for _ in range(P)]
+    if shared_stream:
+        streams = [streams[0]] * P
     bufs = [torch.arange(n, dtype=torch.float32, device="cuda") * (r + 1) / n for r in range(P)]
     host_b = [host(b).copy() for b in bufs]
     torch.cuda.synchronize()
@@ -297,3 +302,37 @@ def test_prepared_calls_from_rank_threads(dt):
         torch.cuda.synchronize()
         for q in range(P):
             assert_same(host(a[q]), host(b[q]), f"allreduce rank {q}")
+
+
+@pytest.mark.parametrize("P", [2, 4, 8])
+def test_rank_local_barrier_orders_data_ring(dt, P):
+    # The barrier page's ordering example from rank threads: each rank stages
+    # its values on its own stream (after a stream sleep of its own length, so
+    # the ranks finish staging at different times), meets the others in a
+    # rank-local barrier, then reads the next rank's stage on its own stream.
+    # Without the barrier's ordering a rank would read a stale stage.
+    n, rounds = 1 << 16, 6
+    streams = [torch.cuda.Stream() for _ in range(P)]
+    stage = [torch.zeros(n, dtype=torch.int32, device="cuda") for _ in range(P)]
+    outs = [[torch.empty(n, dtype=torch.int32, device="cuda") for _ in range(rounds)] for _ in range(P)]
+    vals = [[torch.full((n,), 1000 * k + r, dtype=torch.int32, device="cuda") for k in range(rounds)]
+            for r in range(P)]
+    torch.cuda.synchronize()
+    with group(P) as g:
+        def rank(r):
+            s = streams[r]
+            with torch.cuda.stream(s):
+                for k in range(rounds):
+                    torch.cuda._sleep(200_000 * ((r * 7 + k * 3) % P + 1))
+                    stage[r].copy_(vals[r][k])
+                    dt.dt_barrier(g, r, s)
+                    outs[r][k].copy_(stage[(r + 1) % P])
+                    dt.dt_barrier(g, r, s)       # nobody restages before everyone has read
+        errs = run_ranks(P, rank)
+        assert errs == [None] * P, errs
+        torch.cuda.synchronize()
+        assert dt.dt_group_check(g) == dt.DT_OK
+        assert np.array_equal(dt.dt_debug_read_window(g), oracle.expected_window(P, 2 * rounds))
+    for r in range(P):
+        for k in range(rounds):
+            assert torch.all(outs[r][k] == 1000 * k + (r + 1) % P), f"rank {r} round {k}"
