@@ -251,7 +251,49 @@ def time_oracle_configs(min_seconds: float = 1.0):
     v, reps = rate(lambda: oracle.all_gather(ins, rws, 4096 * 4), sum(rws) * 16384 * 9)
     out["uneven_all_gather_i32_P8"] = {"GB/s": v, "reps": reps,
                                        "sample": f"rows {rws} x 4096 (rows up to 2048)"}
+    out["sweep_bf16_sum_P4"] = time_oracle_sweep()
     return out
+
+
+def time_oracle_sweep(P: int = 4, max_bytes: int = 256 << 20, budget_s: float = 45.0):
+    """The oracle on the size sweep's inputs (uniform [-1, 1) bf16, seed 4):
+    AllReduce and ReduceScatter kSum, AllGather and AllToAll, P = 4, per-rank
+    sizes 4 KiB .. 256 MiB (x4), each the median of 3 single calls; GB/s over
+    the algorithmic bytes the GPU sweep counts.  Stops early (and says so) past
+    budget_s seconds."""
+    import oracle
+    from same_device_collective_gb300 import workloads
+    t_start = time.perf_counter()
+    points = {}
+    stopped = None
+    last = 0.0                                 # seconds the previous size took
+    for nbytes in [b for b in workloads.SWEEP_BYTES if b <= max_bytes]:
+        spent = time.perf_counter() - t_start
+        if spent + 4.5 * last > budget_s:      # the next size moves 4x the bytes
+            stopped = f"time budget of {budget_s:.0f} s reached before {nbytes} B per rank"
+            break
+        t_size = time.perf_counter()
+        w = workloads.sweep_inputs(4, P, nbytes, "bf16")
+        xs = [x.view(__import__("torch").int16).numpy().view(np.uint16) for x in w.inputs]
+        n = xs[0].size
+        cases = {
+            "allreduce": (lambda: oracle.allreduce("bf16", "sum", xs), 2 * P * nbytes),
+            "reduce_scatter": (lambda: oracle.reduce_scatter("bf16", "sum", xs), (P + 1) * nbytes),
+            "all_gather": (lambda: oracle.all_gather(xs), (P + P * P) * nbytes),
+            "all_to_all": (lambda: oracle.all_to_all(xs), 2 * P * nbytes),
+        }
+        for op, (fn, b) in cases.items():
+            ts = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                fn()
+                ts.append(time.perf_counter() - t0)
+            t = sorted(ts)[1]
+            points[f"{op}_{nbytes}B"] = {"GB/s": round(b / t / 1e9, 4), "s": round(t, 6)}
+        del w, xs
+        last = time.perf_counter() - t_size
+    return {"points": points, "P": P, "dtype": "bf16", "op": "sum (reductions)",
+            "timing": "median of 3 single calls, time.perf_counter", "stopped": stopped}
 
 
 def run_reference(args):
@@ -391,6 +433,29 @@ def measure_rows(dt, dev, peak, only=None):
         rec("bucket_allreduce_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
             barriers=nb - 1)
         dt.dt_group_destroy(g)
+        # the allocation-free entry point on the same gradients: device time,
+        # and the host time of one call when it copies its tables (stream idle)
+        # and when it repeats the previous call's tables
+        cap = workloads.BUCKET_CAP_BYTES
+        static = lambda c=cap: dt.dt_bucket_allreduce_static(8, table, cnt, "bf16", "avg", c)
+        ms = time_events(static, 20, reps=STEADY_REPS)
+        copy_us, reuse_us = [], []
+        for i in range(20):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            static(cap - 4096 * (i % 2))           # other buckets than the call before
+            copy_us.append((time.perf_counter() - t0) * 1e6)
+        torch.cuda.synchronize()
+        static()
+        for _ in range(50):
+            t0 = time.perf_counter()
+            static()
+            reuse_us.append((time.perf_counter() - t0) * 1e6)
+        torch.cuda.synchronize()
+        rec("bucket_allreduce_static_avg_bf16_P8_T200", 2 * 8 * sum(counts) * 2, ms, buckets=nb,
+            barriers=0, host_us_tables_copied=round(sorted(copy_us)[len(copy_us) // 2], 1),
+            host_us_tables_reused=round(sorted(reuse_us)[len(reuse_us) // 2], 1),
+            note="no group: stream order between buckets, no signal barrier")
         del w
 
     # A4: AllToAll P=8, bf16 [65536, 4096] per rank

@@ -69,6 +69,28 @@ struct GradRange {
     uintptr_t lo, hi;
 };
 GradRange h_ranges[kStaticScratchBytes / sizeof(void *)];
+
+// One launch per bucket of the tables last built.
+struct Launch {
+    size_t tb, te, start_off;
+    uint64_t total, per_block;
+    uint32_t blocks;
+};
+constexpr size_t kMaxBuckets = 4096;
+Launch g_launches[kMaxBuckets];
+
+// The arguments of the call whose tables the device array holds (with
+// g_last_key): a call that repeats them launches from g_launches without
+// building or comparing its tables.
+constexpr size_t kMaxTensors = kStaticScratchBytes / (sizeof(void *) + sizeof(dt::BucketTensor));
+struct LastCall {
+    bool valid = false;
+    int device = -1, P = 0, dtype = -1;
+    size_t n_tensors = 0, cap = 0, ptr_bytes = 0, tab_bytes = 0, n_launches = 0;
+};
+LastCall g_last_call;
+void *h_last_grads[kStaticScratchBytes / sizeof(void *)];
+size_t h_last_counts[kMaxTensors];
 std::mutex g_static_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
@@ -86,6 +108,30 @@ cudaError_t scratch_address(int device, void **out)
     }
     *out = g_scratch_addr[device];
     return cudaSuccess;
+}
+
+// One kernel per bucket of the tables in the device array d, in order on s.
+// No signal barrier runs between buckets: with no group there is no window,
+// and stream order already orders the buckets.
+dt_status launch_all(const unsigned char *d, size_t ptr_bytes, size_t tab_bytes, size_t nl, int P,
+                     int dtype, int op, int device, cudaStream_t s)
+{
+    dt::BucketParams bp;
+    memset(&bp, 0, sizeof bp);   // win = nullptr: no barrier block
+    bp.ptrs = reinterpret_cast<void *const *>(d);
+    bp.P = P;
+    bp.avg_pow2 = (P & (P - 1)) == 0;
+    bp.avg_scale = bp.avg_pow2 ? 1.0f / (float)P : 0.0f;
+    for (size_t i = 0; i < nl; ++i) {
+        const Launch &L = g_launches[i];
+        bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
+        bp.block_start = reinterpret_cast<const uint32_t *>(d + ptr_bytes + tab_bytes) + L.start_off;
+        bp.ntensors = (uint32_t)(L.te - L.tb);
+        bp.total = L.total;
+        bp.per_block = L.per_block;
+        if (dt::launch_bucket(bp, dtype, op, device, s) != cudaSuccess) return DT_ERR_CUDA;
+    }
+    return DT_OK;
 }
 
 }  // namespace
@@ -123,6 +169,17 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return DT_ERR_CUDA;
 
+    const LastCall &lc = g_last_call;
+    if (lc.valid && lc.device == device && lc.P == P && lc.dtype == dtype && lc.cap == cap &&
+        lc.n_tensors == n_tensors && memcmp(h_last_counts, counts, n_tensors * sizeof(size_t)) == 0 &&
+        memcmp(h_last_grads, grads, n_tensors * P * sizeof(void *)) == 0) {
+        void *scratch = nullptr;
+        if (scratch_address(device, &scratch) != cudaSuccess) return DT_ERR_CUDA;
+        return launch_all(static_cast<const unsigned char *>(scratch), lc.ptr_bytes, lc.tab_bytes,
+                          lc.n_launches, P, dtype, op, device, s);
+    }
+    g_last_call.valid = false;   // the tables are rebuilt below
+
     // plan: [T * P pointers][T tensor entries][block starts of every bucket];
     // buckets are consecutive tensors, greedy in order under the cap (the
     // rule of dt_bucket_plan).  Sizes are checked against the fixed array as
@@ -135,12 +192,7 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
     uint32_t *starts = reinterpret_cast<uint32_t *>(h_bucket_staging + ptr_bytes + tab_bytes);
     const size_t max_starts = (kStaticScratchBytes - ptr_bytes - tab_bytes) / sizeof(uint32_t);
 
-    struct Launch {
-        size_t tb, te, start_off;
-        uint64_t total, per_block;
-        uint32_t blocks;
-    };
-    static Launch launches[4096];   // buckets of this call (guarded by g_static_mu)
+    Launch *const launches = g_launches;   // guarded by g_static_mu
     size_t nl = 0, n_starts = 0;
     size_t t = 0;
     while (t < n_tensors) {
@@ -160,7 +212,7 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
             ++t;
         }
         if (first == 0) continue;   // only empty tensors
-        if (nl == sizeof(launches) / sizeof(launches[0])) return DT_ERR_TOO_LARGE;
+        if (nl == kMaxBuckets) return DT_ERR_TOO_LARGE;
         Launch &L = launches[nl++];
         L.tb = tb;
         L.te = t;
@@ -210,23 +262,9 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
         g_last_key = UploadKey{device, P, dtype, plan_bytes};
     }
 
-    const unsigned char *d = static_cast<const unsigned char *>(scratch);
-    dt::BucketParams bp;
-    memset(&bp, 0, sizeof bp);   // gen = 0: no barrier between buckets
-    bp.ptrs = reinterpret_cast<void *const *>(d);
-    bp.P = P;
-    bp.avg_pow2 = (P & (P - 1)) == 0;
-    bp.avg_scale = bp.avg_pow2 ? 1.0f / (float)P : 0.0f;
-    // one launch per bucket, no signal barrier between buckets: with no group
-    // there is no window, and stream order already orders the buckets
-    for (size_t i = 0; i < nl; ++i) {
-        const Launch &L = launches[i];
-        bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
-        bp.block_start = reinterpret_cast<const uint32_t *>(d + ptr_bytes + tab_bytes) + L.start_off;
-        bp.ntensors = (uint32_t)(L.te - L.tb);
-        bp.total = L.total;
-        bp.per_block = L.per_block;
-        if (dt::launch_bucket(bp, dtype, op, device, s) != cudaSuccess) return DT_ERR_CUDA;
-    }
-    return DT_OK;
+    g_last_call = LastCall{true, device, P, dtype, n_tensors, cap, ptr_bytes, tab_bytes, nl};
+    memcpy(h_last_grads, grads, ptr_bytes);
+    memcpy(h_last_counts, counts, n_tensors * sizeof(size_t));
+    return launch_all(static_cast<const unsigned char *>(scratch), ptr_bytes, tab_bytes, nl, P, dtype,
+                      op, device, s);
 }
