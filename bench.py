@@ -890,6 +890,28 @@ def measure_rows(dt, dev, peak, only=None):
             "GB/s": round(b / (ms1 * 1e-3) / 1e9, 1), "us": round(ms1 * 1e3, 2),
             "aligned_us": round(ms0 * 1e3, 2), "ratio_to_aligned": round(ms0 / ms1, 4),
             "status_ok": ok}
+        # an AllReduce whose inputs start 0, 2, 4, 6 bytes past a boundary
+        # (aligned outputs: the shifting reduction), beside the aligned call
+        n = 32 << 20                              # 64 MiB of bf16 per rank
+        g = dt.dt_group_create(P, dev.index)
+        res = {}
+        for name, offs in (("aligned", (0, 0, 0, 0)), ("inputs_at_own_offsets", (0, 2, 4, 6))):
+            base = [torch.empty(n + 8, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+            xs = [b_[o // 2:o // 2 + n] for b_, o in zip(base, offs)]
+            for x in xs:
+                x.copy_(torch.rand(n, generator=gen, device=dev).to(torch.bfloat16))
+            outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+            res[name] = time_events(lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "bf16", "sum"), 10,
+                                    reps=STEADY_REPS)
+            del base, xs, outs
+        ok = dt.dt_group_check(g) == dt.DT_OK
+        dt.dt_group_destroy(g)
+        b = 2 * P * n * 2
+        ms0, ms1 = res["aligned"], res["inputs_at_own_offsets"]
+        rows["allreduce_bf16_P4_64MiB_inputs_at_own_offsets"] = {
+            "GB/s": round(b / (ms1 * 1e-3) / 1e9, 1), "us": round(ms1 * 1e3, 2),
+            "aligned_us": round(ms0 * 1e3, 2), "ratio_to_aligned": round(ms0 / ms1, 4),
+            "status_ok": ok}
 
     torch.cuda.empty_cache()
     return rows
@@ -972,7 +994,9 @@ NCU_CASES = {
     "all_to_all_2d": ("copy2d_kernel", 2, "AllToAll S(0) -> S(1) bf16, P=8, [8192, 4096] per rank"),
     "small_gather": ("copy_vec_kernel", 2, "AllGather bf16, P=4, 256 KiB shards, per-rank outputs"),
     "reduce_scalar": ("reduce_scalar_kernel", 2,
-                      "AllReduce kSum bf16, P=4, 16 MiB per rank, inputs at different offsets"),
+                      "AllReduce kSum bf16, P=4, 16 MiB per rank, inputs and outputs at different offsets"),
+    "reduce_shift": ("reduce_shift_kernel", 2,
+                     "AllReduce kSum bf16, P=4, 16 MiB per rank, inputs at different offsets, aligned outputs"),
     "shift_gather": ("copy_shift_kernel", 2,
                      "AllGather bf16, P=4, 16 MiB shards 2 bytes past a boundary, aligned outputs"),
 }
@@ -1047,12 +1071,16 @@ def run_ncu_case(name):
         outs = [torch.empty(4 * n, dtype=torch.bfloat16, device=dev) for _ in range(4)]
         g = dt.dt_group_create(4, dev.index)
         call = lambda: dt.dt_all_gather(g, ALL, shards, outs, None, 1, n * 2)
-    elif name == "reduce_scalar":
+    elif name in ("reduce_scalar", "reduce_shift"):
         n = 8 << 20
         gen = torch.Generator(device=dev).manual_seed(4)
         base = [torch.rand(n + 8, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
         xs = [b_[r:r + n] for r, b_ in enumerate(base)]          # offsets 0, 2, 4, 6 bytes
-        outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        if name == "reduce_shift":
+            outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        else:                                                   # outputs apart too
+            obase = [torch.empty(n + 8, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            outs = [b_[r:r + n] for r, b_ in enumerate(obase)]
         g = dt.dt_group_create(4, dev.index)
         call = lambda: dt.dt_allreduce(g, ALL, xs, outs, n, "bf16", "sum")
     else:

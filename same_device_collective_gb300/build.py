@@ -21,9 +21,10 @@ LIB = os.path.join(PKG, "libdt.so")
 # rank-local pattern from native threads, linked against libdt.so
 STEP_TOOL = os.path.join(PKG, "rank_local_step")
 
-SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_copy.cu", "dt_bucket.cu", "dt_barrier.cu",
-           "dt_static.cu"]
-HEADERS = ["dt_internal.h", "dt_group.h", "dt_math.cuh", "dt_device.cuh"]
+SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_reduce_shift.cu", "dt_copy.cu", "dt_bucket.cu",
+           "dt_barrier.cu", "dt_static.cu"]
+HEADERS = ["dt_internal.h", "dt_group.h", "dt_math.cuh", "dt_device.cuh", "dt_shift.cuh",
+           "dt_reduce_shift.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the reductions use

@@ -23,6 +23,7 @@
 
 #include "dt_internal.h"
 #include "dt_device.cuh"
+#include "dt_shift.cuh"
 
 namespace dt {
 namespace {
@@ -214,35 +215,6 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 // discarded.
 constexpr uint64_t kShiftChunks = 512;                 // 8 KiB of destination per tile
 constexpr uint64_t kShiftTile = kShiftChunks * 16;
-
-__device__ __forceinline__ uint4 shift_pair(const uint4 &a, const uint4 &b, uint32_t sh)
-{
-    // bytes [sh, sh + 16) of the 32-byte little-endian sequence a, b
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    const uint32_t bits = (sh & 3) * 8;
-    uint32_t o[4];
-    switch (sh >> 2) {
-#define DT_SHIFT_CASE(q)                                                                  \
-    case q:                                                                               \
-        o[0] = __funnelshift_r(w[q + 0], w[q + 1], bits);                                 \
-        o[1] = __funnelshift_r(w[q + 1], w[q + 2], bits);                                 \
-        o[2] = __funnelshift_r(w[q + 2], w[q + 3], bits);                                 \
-        o[3] = __funnelshift_r(w[q + 3], w[q + 4], bits);                                 \
-        break;
-        DT_SHIFT_CASE(0)
-        DT_SHIFT_CASE(1)
-        DT_SHIFT_CASE(2)
-        DT_SHIFT_CASE(3)
-#undef DT_SHIFT_CASE
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ uint4 shfl_down_uint4(const uint4 &v)
-{
-    return make_uint4(__shfl_down_sync(0xFFFFFFFFu, v.x, 1), __shfl_down_sync(0xFFFFFFFFu, v.y, 1),
-                      __shfl_down_sync(0xFFFFFFFFu, v.z, 1), __shfl_down_sync(0xFFFFFFFFu, v.w, 1));
-}
 
 // Tiles of one (segment, destination) pair: enough for its bytes, at least one.
 __host__ __device__ __forceinline__ uint64_t shift_tiles(uint64_t bytes)

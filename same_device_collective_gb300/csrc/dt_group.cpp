@@ -26,6 +26,7 @@
 #include <vector>
 
 #include "dt_group.h"
+#include "dt_reduce_shift.h"
 
 // Built with -DDT_NVTX (DT_NVTX=1 when building), every public entry point
 // opens an NVTX range named after itself for profiler timelines.
@@ -703,8 +704,18 @@ dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *cons
     p.out_per_job = nout;
     set_avg(P, &p.avg_scale, &p.avg_pow2);
 
+    // Other element-aligned layouts whose outputs share an offset: the
+    // shifting kernel reads the inputs as aligned vectors and shifts them.
+    bool shift = !vec;
+    for (int r = 0; r < P && shift; ++r) shift = ((uintptr_t)in[r] % es) == 0;
+    for (int q = 0; q < nout && shift; ++q)
+        shift = ((uintptr_t)out[q] & 15) == ((uintptr_t)out[0] & 15) && ((uintptr_t)out[q] % es) == 0;
+
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
+    if (shift)
+        return cuda_status(dt::launch_reduce_shift(p, dtype, op, 1, g->device,
+                                                   static_cast<cudaStream_t>(stream)));
     return cuda_status(dt::launch_reduce(p, dtype, op, 1, vec, g->device,
                                          static_cast<cudaStream_t>(stream)));
 }
@@ -768,8 +779,15 @@ dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void 
     p.out_per_job = 1;
     set_avg(P, &p.avg_scale, &p.avg_pow2);
 
+    bool shift = !vec;
+    for (int r = 0; r < P && shift; ++r)
+        shift = ((uintptr_t)in[r] % es) == 0 && ((uintptr_t)out[r] % es) == 0;
+
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
+    if (shift)
+        return cuda_status(dt::launch_reduce_shift(p, dtype, op, P, g->device,
+                                                   static_cast<cudaStream_t>(stream)));
     return cuda_status(dt::launch_reduce(p, dtype, op, P, vec, g->device,
                                          static_cast<cudaStream_t>(stream)));
 }

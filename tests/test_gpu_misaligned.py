@@ -9,7 +9,9 @@ Two layouts reach different kernels:
   the edge bytes alongside;
 - sources and destinations at different offsets (or rows of a byte count
   that is not a multiple of 16): the copies align every store and shift the
-  source into place (a funnel shift across two aligned source vectors).
+  source into place (a funnel shift across two aligned source vectors); the
+  reductions do the same for inputs at their own offsets when the outputs
+  share one, and otherwise reduce element by element.
 Every output sits between two guard zones of a known byte pattern, which must
 survive the call; inputs must be unchanged.
 """
@@ -93,6 +95,47 @@ def test_allreduce_shared_offset(dt, dtype, op, elems_off, n):
         assert gd.intact(), f"guard of rank {q}"
     for (gd, v), s in zip(ins, snap):
         assert np.array_equal(bytes_of(host(v)), bytes_of(s)) and gd.intact()
+
+
+@pytest.mark.parametrize("dtype,op", [("bf16", "avg"), ("bf16", "sum_stepwise"), ("f32", "sum"),
+                                      ("f32", "min"), ("i32", "sum"), ("bf16", "max")])
+@pytest.mark.parametrize("P", [2, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 9, 4099, 100_003])
+@pytest.mark.parametrize("out_layout", ["shared", "apart"])
+def test_allreduce_inputs_at_their_own_offsets(dt, dtype, op, P, n, out_layout):
+    # input r starts (3 r) mod 8 elements past a 16-byte boundary; with the
+    # outputs at one offset the inputs are read as aligned vectors and
+    # shifted into place, with outputs apart the call takes the element path
+    es = ELEM[dtype]
+    xs = rand_inputs(P, n, dtype, 3 * n + P)
+    snap = [host(x).copy() for x in xs]
+    want = oracle.allreduce(dtype, op, snap)
+    ins = [placed(x, (3 * r * es) % 16) for r, x in enumerate(xs)]
+    outs = [empty_at(n * es, TORCH_DTYPE[dtype], (es if out_layout == "shared" else q * es) % 16)
+            for q in range(P)]
+    with group(P) as g:
+        dt.dt_allreduce(g, dt.DT_ALL_RANKS, [v for _, v in ins], [v for _, v in outs], n, dtype, op)
+        torch.cuda.synchronize()
+    for q, (gd, v) in enumerate(outs):
+        assert_same(host(v), want[q], f"rank {q}")
+        assert gd.intact(), f"guard of rank {q}"
+
+
+@pytest.mark.parametrize("dtype,op", [("bf16", "avg"), ("f32", "max"), ("i32", "sum")])
+@pytest.mark.parametrize("P", [2, 5, 16])
+@pytest.mark.parametrize("m", [1, 31, 4093, 20_001])
+def test_reduce_scatter_inputs_at_their_own_offsets(dt, dtype, op, P, m):
+    es = ELEM[dtype]
+    xs = rand_inputs(P, P * m, dtype, 5 * m + P)
+    want = oracle.reduce_scatter(dtype, op, [host(x) for x in xs])
+    ins = [placed(x, (5 * r * es) % 16) for r, x in enumerate(xs)]
+    outs = [empty_at(m * es, TORCH_DTYPE[dtype], (j * es) % 16) for j in range(P)]
+    with group(P) as g:
+        dt.dt_reduce_scatter(g, dt.DT_ALL_RANKS, [v for _, v in ins], [v for _, v in outs], m, dtype, op)
+        torch.cuda.synchronize()
+    for j, (gd, v) in enumerate(outs):
+        assert_same(host(v), want[j], f"shard {j}")
+        assert gd.intact(), f"guard of shard {j}"
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
