@@ -1096,6 +1096,99 @@ def run_ncu_case(name):
     return 0 if st == dt.DT_OK else 1
 
 
+def summarize_timeline(rec, dt):
+    """Per launch (grouped by grid id, in order of their first block's wait):
+    kind, blocks, when work started and ended, and the gaps between launches;
+    for a bucket kernel also its drain and ramp and its barrier block."""
+    import numpy as np
+    out = []
+    grids = {}
+    for r in rec:
+        grids.setdefault(int(r["grid"]), []).append(r)
+    launches = []
+    for gid, rs in grids.items():
+        rs = np.array(rs, dtype=rec.dtype)
+        data = rs[rs["kind"] != 8]
+        bar = rs[rs["kind"] == 8]
+        if data.size == 0:
+            continue
+        ends = np.sort(data["t_end"].astype(np.int64))
+        launches.append({
+            "kind": dt.TIMELINE_KINDS.get(int(data["kind"][0]), str(int(data["kind"][0]))),
+            "blocks": int(data.size),
+            "work_start": int(data["t_waited"].min()), "work_end": int(ends[-1]),
+            "first_end": int(ends[0]), "p90_end": int(ends[int(0.9 * (ends.size - 1))]),
+            "barrier_end": int(bar["t_end"].max()) if bar.size else None})
+    launches.sort(key=lambda x: x["work_start"])
+    if not launches:
+        return {"launches": 0}
+    t0 = launches[0]["work_start"]
+    prev = None
+    for L in launches:
+        e = {"kind": L["kind"], "blocks": L["blocks"],
+             "start_us": round((L["work_start"] - t0) / 1e3, 3),
+             "span_us": round((L["work_end"] - L["work_start"]) / 1e3, 3),
+             "ramp_us": round((L["first_end"] - L["work_start"]) / 1e3, 3),
+             "drain_us": round((L["work_end"] - L["p90_end"]) / 1e3, 3)}
+        if L["barrier_end"] is not None:
+            e["barrier_after_last_block_us"] = round((L["barrier_end"] - L["work_end"]) / 1e3, 3)
+        if prev is not None:
+            last = prev["barrier_end"] if prev["barrier_end"] is not None else prev["work_end"]
+            e["gap_from_previous_us"] = round((L["work_start"] - last) / 1e3, 3)
+        out.append(e)
+        prev = L
+    return {"launches": len(out), "per_launch": out}
+
+
+def run_timeline(name):
+    """A few calls of one workload on a library built with DT_TIMELINE=1, and
+    the per-launch summary of their block timeline (one JSON line)."""
+    import torch
+    from same_device_collective_gb300 import dt, workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ALL = dt.DT_ALL_RANKS
+    try:
+        dt.dt_timeline_start(1 << 20)
+    except dt.DtError as ex:
+        print(json.dumps({"timeline": name, "unavailable": f"{ex} (build with DT_TIMELINE=1)"}))
+        return 1
+    if name == "bucket":
+        w = workloads.bucket_grads(device=str(dev))
+        table = dt.pointer_table(w.inputs)
+        cnt = np.asarray(w.meta["counts"], dtype=np.uint64)
+        g = dt.dt_group_create(8, dev.index)
+        call = lambda: dt.dt_bucket_allreduce(g, table, cnt, "bf16", "avg", workloads.BUCKET_CAP_BYTES)
+        what = "bucket AllReduce kAvg bf16, P=8, 200 tensors, 25 MiB buckets: the third of 3 calls"
+    elif name == "step":
+        P, R, C = P_RANKS, ROWS, COLS
+        w = workloads.rs_ag(seed=1, P=P, rows=R, cols=C, device=str(dev))
+        rs = [torch.empty(R // P, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ag = [torch.empty(R, C, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        g = dt.dt_group_create(P, dev.index)
+
+        def call():
+            dt.dt_barrier(g)
+            dt.dt_reduce_scatter(g, ALL, w.inputs, rs, R // P * C, "bf16", "avg")
+            dt.dt_barrier(g)
+            dt.dt_all_gather(g, ALL, rs, ag, None, R // P, C * 2)
+        what = "RS(avg)+AG step with barriers, P=4, bf16 [8192, 4096]: the third of 3 steps"
+    else:
+        raise ValueError(name)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    dt.dt_timeline_start(1 << 20)
+    torch.cuda._sleep(2_000_000)               # the host enqueues the call before it runs
+    call()
+    rec, n = dt.dt_timeline_read(1 << 20)
+    ok = dt.dt_group_check(g) == dt.DT_OK
+    dt.dt_group_destroy(g)
+    print(json.dumps({"timeline": name, "what": what, "records": n, "status_ok": ok,
+                      **summarize_timeline(rec, dt)}))
+    return 0 if ok else 1
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -1369,6 +1462,8 @@ def main(argv=None):
                     help="measure one collective at its own workload and print it")
     ap.add_argument("--ncu-case", choices=sorted(NCU_CASES),
                     help="run a few calls of one collective for an ncu capture (no timing)")
+    ap.add_argument("--timeline", choices=["bucket", "step"],
+                    help="per-block kernel timeline of one call (a DT_TIMELINE=1 build)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1378,6 +1473,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.ncu_case:
         return run_ncu_case(args.ncu_case)
+    if args.timeline:
+        return run_timeline(args.timeline)
     if args.row:
         import torch
         from same_device_collective_gb300 import dt

@@ -355,6 +355,41 @@ dt_status dt_debug_ring_after_barrier(dt_group_t g, const void *const *in,
  * in the error word and the kernel returns; the GPU stays usable. */
 dt_status dt_debug_barrier_expect(dt_group_t g, int extra, uint32_t timeout_ms, void *stream);
 
+/* ------------------------------------------------------------- tracing */
+
+/* Per-block timeline of the library's kernels, recorded only by a library
+ * built with DT_TIMELINE=1 in the environment (elsewhere both calls return
+ * DT_ERR_UNSUPPORTED).  The pages trace collectives with profiler timelines
+ * ("通信与互联（05）" §六: the communication kernels of each stream on their
+ * own row); this records, for every thread block of every kernel launched
+ * after dt_timeline_start, when it started, when it passed its wait on the
+ * previous kernel (the bucket barrier block: when its barrier completed) and
+ * when it ended, in %globaltimer nanoseconds.
+ *   dt_timeline_start  (re)allocates room for max_records on the current
+ *                      device and empties it; the last one wins
+ *   dt_timeline_read   waits for the device, copies up to max_records records
+ *                      to host memory and sets *n_records; records past the
+ *                      room are dropped and counted in *n_records */
+#define DT_TL_REDUCE 1          /* AllReduce / ReduceScatter, vector kernel */
+#define DT_TL_REDUCE_SHIFT 2    /* the same, inputs at their own offsets */
+#define DT_TL_COPY_BULK 3       /* AllGather / AllToAll, TMA bulk copies */
+#define DT_TL_COPY_VEC 4        /* small copies */
+#define DT_TL_COPY_SHIFT 5      /* copies at other offsets */
+#define DT_TL_COPY_2D 6         /* AllToAll along other dims */
+#define DT_TL_BUCKET 7          /* bucket all-reduce, data block */
+#define DT_TL_BUCKET_BARRIER 8  /* bucket all-reduce, the barrier block after a bucket */
+#define DT_TL_BARRIER 9         /* signal-window barrier kernel */
+typedef struct {
+    uint64_t grid;       /* the launch's %gridid */
+    uint32_t kind;       /* DT_TL_* */
+    uint32_t block;      /* blockIdx.x + gridDim.x * blockIdx.y */
+    uint32_t sm;         /* %smid */
+    uint32_t pad;
+    uint64_t t_start, t_waited, t_end;
+} dt_timeline_record;
+dt_status dt_timeline_start(size_t max_records);
+dt_status dt_timeline_read(dt_timeline_record *out, size_t max_records, size_t *n_records);
+
 #ifdef __cplusplus
 }
 #endif

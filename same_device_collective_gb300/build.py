@@ -24,7 +24,7 @@ STEP_TOOL = os.path.join(PKG, "rank_local_step")
 SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_reduce_shift.cu", "dt_copy.cu", "dt_bucket.cu",
            "dt_barrier.cu", "dt_static.cu"]
 HEADERS = ["dt_internal.h", "dt_group.h", "dt_math.cuh", "dt_device.cuh", "dt_shift.cuh",
-           "dt_reduce_shift.h"]
+           "dt_reduce_shift.h", "dt_timeline.cuh", "dt_timeline.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the reductions use
@@ -36,6 +36,11 @@ NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC
 if os.environ.get("DT_NVTX") == "1":
     NVFLAGS.append("-DDT_NVTX")
     BUILD = BUILD + "_nvtx"
+# DT_TIMELINE=1: every kernel block records its start, wait and end times
+# (dt_timeline_start / dt_timeline_read); its objects live in their own folder.
+if os.environ.get("DT_TIMELINE") == "1":
+    NVFLAGS.append("-DDT_TIMELINE")
+    BUILD = BUILD + "_timeline"
 
 
 def nvcc() -> str:

@@ -22,6 +22,7 @@
 // error word and its host-mapped mirror and returns, so the GPU is never held.
 #include "dt_internal.h"
 #include "dt_device.cuh"
+#include "dt_timeline.cuh"
 
 namespace dt {
 namespace {
@@ -95,8 +96,11 @@ __device__ bool rank_barrier(const BarrierParams &p, int r)
 // One block of 32 * P threads: warp r is rank r.
 __global__ void __launch_bounds__(32 * DT_MAX_RANKS) barrier_kernel(const __grid_constant__ BarrierParams p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     rank_barrier<false>(p, threadIdx.x >> 5);
+    DT_TL_END_BLOCK(DT_TL_BARRIER);
 }
 
 __device__ void copy_bytes(unsigned char *dst, const unsigned char *src, uint64_t n)
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ 
 }
 
 }  // namespace
+
+DT_TL_BINDER(bind_timeline_barrier)
 
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s)
 {

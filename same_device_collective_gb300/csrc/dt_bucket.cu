@@ -14,6 +14,7 @@
 #include "dt_internal.h"
 #include "dt_device.cuh"
 #include "dt_math.cuh"
+#include "dt_timeline.cuh"
 
 namespace dt {
 namespace {
@@ -126,9 +127,12 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     // the call's first kernel in stream order, and no kernel writes it.  The
     // gradients themselves are touched only after griddepcontrol.wait.  This
     // takes two dependent table reads off the start of every bucket.
+    DT_TL_BEGIN();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (p.win && blockIdx.x == gridDim.x - 1) {
         bucket_barrier_block(p);
+        DT_TL_WAITED();
+        DT_TL_END_BLOCK(DT_TL_BUCKET_BARRIER);
         return;
     }
     const uint64_t lo = (uint64_t)blockIdx.x * p.per_block;
@@ -143,6 +147,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)(bt.slot & 0x7FFFFFFFu) * P + threadIdx.x];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
+    DT_TL_WAITED();
 
     for (;;) {
         const uint64_t s = (lo > bt.first ? lo : bt.first) - bt.first;   // local range [s, e)
@@ -187,6 +192,7 @@ bucket_kernel(const __grid_constant__ BucketParams p)
         __syncthreads();
     }
     count_out(p);
+    DT_TL_END_BLOCK(DT_TL_BUCKET);
 }
 
 using BucketFn = void (*)(BucketParams);
@@ -209,6 +215,8 @@ BucketFn pick_fn(int dtype, int op, int P)
 }
 
 }  // namespace
+
+DT_TL_BINDER(bind_timeline_bucket)
 
 uint64_t bucket_padded(uint64_t count, int dtype)
 {

@@ -24,6 +24,7 @@
 #include "dt_internal.h"
 #include "dt_device.cuh"
 #include "dt_shift.cuh"
+#include "dt_timeline.cuh"
 
 namespace dt {
 namespace {
@@ -148,7 +149,9 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     constexpr int kBulkStages = BulkShape<KIND>::kStages;
     constexpr int kBulkTile = BulkShape<KIND>::kTile;
     extern __shared__ __align__(128) unsigned char smem[];
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     if (threadIdx.x != 0) return;
     const uint64_t first = blockIdx.x, step = gridDim.x;
     if (first >= p.total_tiles) return;
@@ -199,6 +202,7 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         }
     }
     bulk_wait_all();
+    DT_TL_END_THREAD(DT_TL_COPY_BULK);
 }
 
 // Any alignment: the destination is cut into tiles of kShiftChunks 16-byte
@@ -227,7 +231,9 @@ template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kThreads)
 copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         const CopySeg &sg = p.seg[find_seg(p, tile)];
@@ -273,6 +279,7 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
             }
         }
     }
+    DT_TL_END_BLOCK(DT_TL_COPY_SHIFT);
 }
 
 // Small aligned launches: plain 16-byte loads and stores, two vectors per
@@ -298,7 +305,9 @@ template <int NSEG, int NOUT>
 __global__ void __launch_bounds__(kThreads)
 copy_vec_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         const CopySeg &sg = p.seg[find_seg(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
@@ -320,6 +329,7 @@ copy_vec_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
             }
         }
     }
+    DT_TL_END_BLOCK(DT_TL_COPY_VEC);
 }
 
 template <int NSEG, int NOUT, int KIND>
@@ -486,6 +496,8 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
 
 }  // namespace
 
+DT_TL_BINDER(bind_timeline_copy)
+
 cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
                         const ErrorSink &sink, int device, cudaStream_t s)
 {
@@ -506,7 +518,9 @@ namespace {
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant__ Copy2dParams p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         const Copy2dSeg &sg = p.seg[find_seg(p, tile)];
@@ -525,6 +539,7 @@ __global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant_
             }
         }
     }
+    DT_TL_END_BLOCK(DT_TL_COPY_2D);
 }
 
 }  // namespace

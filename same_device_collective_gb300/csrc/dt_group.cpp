@@ -27,6 +27,7 @@
 
 #include "dt_group.h"
 #include "dt_reduce_shift.h"
+#include "dt_timeline.h"
 
 // Built with -DDT_NVTX (DT_NVTX=1 when building), every public entry point
 // opens an NVTX range named after itself for profiler timelines.
@@ -1453,6 +1454,74 @@ dt_status dt_debug_barrier_expect(dt_group_t g, int extra, uint32_t timeout_ms, 
     if (e != cudaSuccess) return cuda_status(e);
     g->barriers_issued++;
     return DT_OK;
+}
+
+// ---- tracing (DT_TIMELINE=1 builds) ------------------------------------------
+
+#ifdef DT_TIMELINE
+namespace {
+std::mutex g_tl_mu;
+dt_timeline_record *g_tl_rec = nullptr;
+unsigned long long *g_tl_count = nullptr;
+size_t g_tl_cap = 0;
+int g_tl_device = -1;
+}  // namespace
+#endif
+
+dt_status dt_timeline_start(size_t max_records)
+{
+#ifdef DT_TIMELINE
+    if (max_records == 0 || max_records > ((size_t)1 << 28)) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_tl_mu);
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return DT_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DT_ERR_CUDA;
+    if (g_tl_rec) cudaFree(g_tl_rec);
+    if (g_tl_count) cudaFree(g_tl_count);
+    g_tl_rec = nullptr;
+    g_tl_count = nullptr;
+    cudaError_t e = cudaMalloc(&g_tl_rec, max_records * sizeof(dt_timeline_record));
+    if (e == cudaSuccess) e = cudaMalloc(&g_tl_count, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMemset(g_tl_count, 0, sizeof(unsigned long long));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? DT_ERR_OOM : DT_ERR_CUDA;
+    g_tl_cap = max_records;
+    g_tl_device = device;
+    const dt::TimelineSink sink{g_tl_rec, g_tl_count, (unsigned long long)max_records};
+    dt::bind_timeline_reduce(&sink);
+    dt::bind_timeline_reduce_shift(&sink);
+    dt::bind_timeline_copy(&sink);
+    dt::bind_timeline_bucket(&sink);
+    dt::bind_timeline_barrier(&sink);
+    return cudaDeviceSynchronize() == cudaSuccess ? DT_OK : DT_ERR_CUDA;
+#else
+    (void)max_records;
+    return DT_ERR_UNSUPPORTED;
+#endif
+}
+
+dt_status dt_timeline_read(dt_timeline_record *out, size_t max_records, size_t *n_records)
+{
+#ifdef DT_TIMELINE
+    if (!n_records || (max_records && !out)) return DT_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_tl_mu);
+    if (!g_tl_rec) return DT_ERR_INVALID;
+    DeviceScope scope(g_tl_device);
+    if (!scope.ok || cudaDeviceSynchronize() != cudaSuccess) return DT_ERR_CUDA;
+    unsigned long long n = 0;
+    if (cudaMemcpy(&n, g_tl_count, sizeof n, cudaMemcpyDeviceToHost) != cudaSuccess) return DT_ERR_CUDA;
+    *n_records = (size_t)n;
+    size_t k = n < g_tl_cap ? (size_t)n : g_tl_cap;
+    if (k > max_records) k = max_records;
+    if (k && cudaMemcpy(out, g_tl_rec, k * sizeof(dt_timeline_record), cudaMemcpyDeviceToHost) !=
+                 cudaSuccess)
+        return DT_ERR_CUDA;
+    return DT_OK;
+#else
+    (void)out;
+    (void)max_records;
+    (void)n_records;
+    return DT_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -19,6 +19,7 @@
 #include "dt_internal.h"
 #include "dt_device.cuh"
 #include "dt_math.cuh"
+#include "dt_timeline.cuh"
 
 namespace dt {
 namespace {
@@ -38,7 +39,9 @@ template <int DT, int OP, int PMAX, int U>
 __global__ void __launch_bounds__(kThreads)
 reduce_vec_kernel(const __grid_constant__ ReduceParams p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     const int P = p.P;
     const int j = blockIdx.y;
@@ -80,6 +83,7 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
             reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)threadIdx.x - (int64_t)p.head, P, dst, ndst,
                                 p.avg_scale, p.avg_pow2);
     }
+    DT_TL_END_BLOCK(DT_TL_REDUCE);
 }
 
 // Any alignment: element by element, same arithmetic.
@@ -144,6 +148,8 @@ KernelInfo pick_op(int op, int P, bool vec, bool scatter)
 }
 
 }  // namespace
+
+DT_TL_BINDER(bind_timeline_reduce)
 
 constexpr int kGridPerResident = 8;
 

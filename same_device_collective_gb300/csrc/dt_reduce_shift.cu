@@ -17,6 +17,7 @@
 #include "dt_math.cuh"
 #include "dt_reduce_shift.h"
 #include "dt_shift.cuh"
+#include "dt_timeline.cuh"
 
 namespace dt {
 namespace {
@@ -25,7 +26,9 @@ template <int DT, int OP, int PMAX>
 __global__ void __launch_bounds__(kThreads)
 reduce_shift_kernel(const __grid_constant__ ReduceParams p)
 {
+    DT_TL_BEGIN();
     pdl_begin();
+    DT_TL_WAITED();
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     constexpr int ES = 16 / EPV;
     constexpr int kChunksPerWarp = 31;
@@ -82,6 +85,7 @@ reduce_shift_kernel(const __grid_constant__ ReduceParams p)
         for (uint64_t i = dh + nch * EPV + threadIdx.x; i < p.n; i += kThreads)
             reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
     }
+    DT_TL_END_BLOCK(DT_TL_REDUCE_SHIFT);
 }
 
 using ShiftFn = void (*)(ReduceParams);
@@ -113,6 +117,8 @@ ShiftFn pick_op(int op, int P)
 }
 
 }  // namespace
+
+DT_TL_BINDER(bind_timeline_reduce_shift)
 
 cudaError_t launch_reduce_shift(const ReduceParams &p, int dtype, int op, int jobs, int device,
                                 cudaStream_t s)

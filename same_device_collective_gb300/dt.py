@@ -79,11 +79,21 @@ _SIGS = {
     "dt_debug_read_window": ([_vp, ctypes.POINTER(ctypes.c_int32), _vp], _i),
     "dt_debug_ring_after_barrier": ([_vp, _vpp, _vpp, _vpp, _sz, _vp], _i),
     "dt_debug_barrier_expect": ([_vp, _i, _u32, _vp], _i),
+    "dt_timeline_start": ([_sz], _i),
+    "dt_timeline_read": ([_vp, _sz, _szp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = _res
+
+
+# dt_timeline_record of include/dt.h (48 bytes)
+TIMELINE_DTYPE = np.dtype([("grid", np.uint64), ("kind", np.uint32), ("block", np.uint32),
+                           ("sm", np.uint32), ("pad", np.uint32), ("t_start", np.uint64),
+                           ("t_waited", np.uint64), ("t_end", np.uint64)])
+TIMELINE_KINDS = {1: "reduce", 2: "reduce_shift", 3: "copy_bulk", 4: "copy_vec", 5: "copy_shift",
+                  6: "copy_2d", 7: "bucket", 8: "bucket_barrier", 9: "barrier"}
 
 
 class DtError(RuntimeError):
@@ -190,6 +200,20 @@ def dt_status_string(status: int) -> str:
 
 def dt_launch_count() -> int:
     return int(_lib.dt_launch_count())
+
+
+def dt_timeline_start(max_records: int) -> None:
+    """Start recording the kernel timeline (a DT_TIMELINE=1 build; raises
+    DtError DT_ERR_UNSUPPORTED otherwise)."""
+    _check(_lib.dt_timeline_start(max_records), "dt_timeline_start")
+
+
+def dt_timeline_read(max_records: int):
+    """(records as a numpy array of TIMELINE_DTYPE, number recorded)."""
+    out = np.zeros(max_records, dtype=TIMELINE_DTYPE)
+    n = ctypes.c_size_t()
+    _check(_lib.dt_timeline_read(out.ctypes.data, max_records, ctypes.byref(n)), "dt_timeline_read")
+    return out[:min(n.value, max_records)], n.value
 
 
 def dt_group_create(world_size: int, cuda_device: int = 0) -> int:

@@ -137,3 +137,28 @@ def test_prepared_calls_make_the_same_call_as_the_functions(dt):
         dt.prepare(dt.dt_status_string, 0)
     with pytest.raises(ValueError):
         dt.prepare(print, 0)
+
+
+def test_timeline_is_unsupported_in_the_default_build(dt):
+    # Only a DT_TIMELINE=1 build records the kernel timeline; the default one
+    # answers without touching a device.
+    lib = dt.library()
+    assert lib.dt_timeline_start(16) == dt.DT_ERR_UNSUPPORTED
+    n = ctypes.c_size_t()
+    assert lib.dt_timeline_read(None, 0, ctypes.byref(n)) == dt.DT_ERR_UNSUPPORTED
+    assert dt.TIMELINE_DTYPE.itemsize == 48
+
+
+def test_timeline_flavour_compiles(tmp_path):
+    # DT_TIMELINE=1 builds instrument the kernels; the host unit and the
+    # smallest kernel unit must compile that way (scratch objects only).
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    from same_device_collective_gb300 import build as b
+    for src, lang in (("dt_group.cpp", []), ("dt_barrier.cu", ["-x", "cu"])):
+        cmd = [b.nvcc(), *b.ARCH, "-O1", "-std=c++17", "-Xcompiler", "-fPIC", "-DDT_TIMELINE",
+               "-I", os.path.join(root, "include"), "-I", b.CSRC, *lang, "-c",
+               os.path.join(b.CSRC, src), "-o", str(tmp_path / (src + ".o"))]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
