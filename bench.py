@@ -360,6 +360,119 @@ ROW_NAMES = ["allreduce_small", "allreduce_large", "bucket", "all_to_all", "unev
              "barrier", "rank_local", "placements", "hsdp_pipeline", "sweep_points", "misaligned"]
 
 
+class HsdpSchedule:
+    """The hyper-parallel post_backward schedule on a 2 x 2 mesh of logical
+    ranks (two shard groups, two replicate groups), 8 modules of bf16
+    gradients (32 Mi elements per rank per module); each module's backward
+    compute is stood in for by a bf16 GEMM on the compute stream.  sequential:
+    compute, ReduceScatter, AllReduce per module on one stream; pipelined: the
+    same work with the collectives in async scopes on the groups' own streams
+    (wait previous RS, issue RS, issue previous AR).  `mark`, when given, is
+    called with (stream, tag) before (tag 2m) and after (2m + 1) module m's
+    GEMM."""
+
+    def __init__(self, dt, dev, M=8, n=32 << 20):
+        import torch
+        self.dt, self.M, self.n = dt, M, n
+        gen = torch.Generator(device=dev).manual_seed(7)
+        self.grads = [[torch.randn(n, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
+                      for _ in range(M)]
+        self.rsb = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+                    for _ in range(M)]
+        self.fin = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+                    for _ in range(M)]
+        self.a = torch.randn(8192, 8192, generator=gen, device=dev).to(torch.bfloat16)
+        self.b = torch.randn(8192, 4096, generator=gen, device=dev).to(torch.bfloat16)
+        self.c = torch.empty(8192, 4096, dtype=torch.bfloat16, device=dev)
+        self.shard = [dt.dt_group_create(2, dev.index) for _ in range(2)]
+        self.repl = [dt.dt_group_create(2, dev.index) for _ in range(2)]
+        self.compute = torch.cuda.Stream(dev)
+        self.craw = self.compute.cuda_stream
+        self.comm_bytes = M * 2 * ((2 + 1) * n * 2 + 2 * 2 * (n // 2) * 2)
+        self.mark = None
+
+    def gemm(self, m):
+        import torch
+        if self.mark:
+            self.mark(self.craw, 2 * m)
+        torch.matmul(self.a, self.b, out=self.c)
+        if self.mark:
+            self.mark(self.craw, 2 * m + 1)
+
+    def rs_of(self, m, stream):
+        for s_ in range(2):
+            self.rs_of_one(m, s_, stream)
+
+    def ar_of(self, m, stream):
+        for k in range(2):
+            self.ar_of_one(m, k, stream)
+
+    def gemm_only(self):
+        import torch
+        with torch.cuda.stream(self.compute):
+            for m in range(self.M):
+                self.gemm(m)
+
+    def sequential(self):
+        import torch
+        with torch.cuda.stream(self.compute):
+            for m in range(self.M):
+                self.gemm(m)
+                self.rs_of(m, self.craw)
+                self.ar_of(m, self.craw)
+
+    def pipelined(self):
+        import torch
+        dt = self.dt
+        with torch.cuda.stream(self.compute):
+            prev, pend = [], []
+            for m in range(self.M):
+                self.gemm(m)                                   # module m's backward
+                for w_ in prev:
+                    dt.dt_work_wait(w_, self.compute)
+                    dt.dt_work_free(w_)
+                cur = []
+                for s_ in range(2):
+                    cs = dt.dt_async_begin(self.shard[s_], self.compute)
+                    self.rs_of_one(m, s_, cs)
+                    cur.append(dt.dt_async_end(self.shard[s_]))
+                if m > 0:
+                    for k in range(2):
+                        cs = dt.dt_async_begin(self.repl[k], self.compute)
+                        self.ar_of_one(m - 1, k, cs)
+                        pend.append(dt.dt_async_end(self.repl[k]))
+                prev = cur
+            for w_ in prev:
+                dt.dt_work_wait(w_, self.compute)
+                dt.dt_work_free(w_)
+            for k in range(2):
+                cs = dt.dt_async_begin(self.repl[k], self.compute)
+                self.ar_of_one(self.M - 1, k, cs)
+                pend.append(dt.dt_async_end(self.repl[k]))
+            for w_ in pend:
+                dt.dt_work_wait(w_, self.compute)
+                dt.dt_work_free(w_)
+
+    def rs_of_one(self, m, s_, stream):
+        dt, n = self.dt, self.n
+        x, y = 2 * s_, 2 * s_ + 1
+        dt.dt_reduce_scatter(self.shard[s_], dt.DT_ALL_RANKS, [self.grads[m][x], self.grads[m][y]],
+                             [self.rsb[m][x], self.rsb[m][y]], n // 2, "bf16", "avg", stream)
+
+    def ar_of_one(self, m, k, stream):
+        dt, n = self.dt, self.n
+        dt.dt_allreduce(self.repl[k], dt.DT_ALL_RANKS, [self.rsb[m][k], self.rsb[m][k + 2]],
+                        [self.fin[m][k], self.fin[m][k + 2]], n // 2, "bf16", "avg", 0, stream)
+
+    def close(self):
+        import torch
+        torch.cuda.synchronize()
+        ok = all(self.dt.dt_group_check(x) == self.dt.DT_OK for x in self.shard + self.repl)
+        for x in self.shard + self.repl:
+            self.dt.dt_group_destroy(x)
+        return ok
+
+
 def measure_rows(dt, dev, peak, only=None):
     """One measurement per collective at its own workload (device-resident).
     `only` restricts it to one of ROW_NAMES."""
@@ -684,71 +797,7 @@ def measure_rows(dt, dev, peak, only=None):
     # Pipelined: the same work with the collectives in async scopes on the
     # groups' own streams (wait previous RS, issue RS, issue previous AR).
     if want("hsdp_pipeline"):
-        M, n = 8, 32 << 20
-        gen = torch.Generator(device=dev).manual_seed(7)
-        grads = [[torch.randn(n, generator=gen, device=dev).to(torch.bfloat16) for _ in range(4)]
-                 for _ in range(M)]
-        rsb = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)] for _ in range(M)]
-        fin = [[torch.empty(n // 2, dtype=torch.bfloat16, device=dev) for _ in range(4)] for _ in range(M)]
-        a = torch.randn(8192, 8192, generator=gen, device=dev).to(torch.bfloat16)
-        b = torch.randn(8192, 4096, generator=gen, device=dev).to(torch.bfloat16)
-        c = torch.empty(8192, 4096, dtype=torch.bfloat16, device=dev)
-        shard = [dt.dt_group_create(2, dev.index) for _ in range(2)]
-        repl = [dt.dt_group_create(2, dev.index) for _ in range(2)]
-        compute = torch.cuda.Stream(dev)
-        craw = compute.cuda_stream
-
-        def rs_of(m, stream):
-            for s_ in range(2):
-                x, y = 2 * s_, 2 * s_ + 1
-                dt.dt_reduce_scatter(shard[s_], ALL, [grads[m][x], grads[m][y]],
-                                     [rsb[m][x], rsb[m][y]], n // 2, "bf16", "avg", stream)
-
-        def ar_of(m, stream):
-            for k in range(2):
-                dt.dt_allreduce(repl[k], ALL, [rsb[m][k], rsb[m][k + 2]], [fin[m][k], fin[m][k + 2]],
-                                n // 2, "bf16", "avg", 0, stream)
-
-        def sequential():
-            with torch.cuda.stream(compute):
-                for m in range(M):
-                    torch.matmul(a, b, out=c)
-                    rs_of(m, craw)
-                    ar_of(m, craw)
-
-        def pipelined():
-            with torch.cuda.stream(compute):
-                prev, pend = [], []
-                for m in range(M):
-                    torch.matmul(a, b, out=c)                  # module m's backward
-                    for w_ in prev:
-                        dt.dt_work_wait(w_, compute)
-                        dt.dt_work_free(w_)
-                    cur = []
-                    for s_ in range(2):
-                        cs = dt.dt_async_begin(shard[s_], compute)
-                        x, y = 2 * s_, 2 * s_ + 1
-                        dt.dt_reduce_scatter(shard[s_], ALL, [grads[m][x], grads[m][y]],
-                                             [rsb[m][x], rsb[m][y]], n // 2, "bf16", "avg", cs)
-                        cur.append(dt.dt_async_end(shard[s_]))
-                    if m > 0:
-                        for k in range(2):
-                            cs = dt.dt_async_begin(repl[k], compute)
-                            dt.dt_allreduce(repl[k], ALL, [rsb[m - 1][k], rsb[m - 1][k + 2]],
-                                            [fin[m - 1][k], fin[m - 1][k + 2]], n // 2, "bf16", "avg", 0, cs)
-                            pend.append(dt.dt_async_end(repl[k]))
-                    prev = cur
-                for w_ in prev:
-                    dt.dt_work_wait(w_, compute)
-                    dt.dt_work_free(w_)
-                for k in range(2):
-                    cs = dt.dt_async_begin(repl[k], compute)
-                    dt.dt_allreduce(repl[k], ALL, [rsb[M - 1][k], rsb[M - 1][k + 2]],
-                                    [fin[M - 1][k], fin[M - 1][k + 2]], n // 2, "bf16", "avg", 0, cs)
-                    pend.append(dt.dt_async_end(repl[k]))
-                for w_ in pend:
-                    dt.dt_work_wait(w_, compute)
-                    dt.dt_work_free(w_)
+        h = HsdpSchedule(dt, dev)
 
         def wall(fn, reps=5):
             fn()
@@ -761,25 +810,17 @@ def measure_rows(dt, dev, peak, only=None):
                 ts.append(time.perf_counter() - t0)
             return sorted(ts)[reps // 2]
 
-        def gemm_only():
-            with torch.cuda.stream(compute):
-                for _ in range(M):
-                    torch.matmul(a, b, out=c)
-
-        t_gemm = wall(gemm_only)
-        t_seq = wall(sequential)
-        t_pipe = wall(pipelined)
-        ok = all(dt.dt_group_check(x) == dt.DT_OK for x in shard + repl)
-        for x in shard + repl:
-            dt.dt_group_destroy(x)
-        comm_bytes = M * 2 * ((2 + 1) * n * 2 + 2 * 2 * (n // 2) * 2)
+        t_gemm = wall(h.gemm_only)
+        t_seq = wall(h.sequential)
+        t_pipe = wall(h.pipelined)
+        ok = h.close()
         rows["hsdp_pipeline_2x2_bf16_M8"] = {
             "us_sequential": round(t_seq * 1e6, 1), "us_pipelined": round(t_pipe * 1e6, 1),
             "us_compute_only": round(t_gemm * 1e6, 1),
             "speedup": round(t_seq / t_pipe, 3),
-            "comm_GB/s_sequential_excl_compute": round(comm_bytes / max(t_seq - t_gemm, 1e-9) / 1e9, 1),
+            "comm_GB/s_sequential_excl_compute": round(h.comm_bytes / max(t_seq - t_gemm, 1e-9) / 1e9, 1),
             "status_ok": ok, "timing": "wall clock, median of 5, synchronised"}
-        del grads, rsb, fin, a, b, c
+        del h
 
     # Size sweep (config 5) at the message sizes the HBM target is stated
     # for: every op at P = 2 and P = 16, bf16 kSum, 64 MiB and 256 MiB per
@@ -1140,6 +1181,38 @@ def summarize_timeline(rec, dt):
     return {"launches": len(out), "per_launch": out}
 
 
+def summarize_overlap(rec, dt):
+    """Compute intervals from the marks around each GEMM (tags 2m, 2m + 1) and
+    the collectives' launches: how much of the collectives' block time falls
+    inside a GEMM interval."""
+    import numpy as np
+    marks = rec[rec["kind"] == 10]
+    by_tag = {int(m["block"]): int(m["t_end"]) for m in marks}
+    gemms = sorted((by_tag[2 * m], by_tag[2 * m + 1]) for m in range(len(by_tag) // 2)
+                   if 2 * m in by_tag and 2 * m + 1 in by_tag)
+    coll = rec[(rec["kind"] != 10) & (rec["kind"] != 8)]
+    grids = {}
+    for r in coll:
+        grids.setdefault(int(r["grid"]), []).append(r)
+    spans = sorted((int(np.min([x["t_waited"] for x in v])), int(np.max([x["t_end"] for x in v])))
+                   for v in grids.values())
+
+    def overlap(a, b):
+        return max(0, min(a[1], b[1]) - max(a[0], b[0]))
+
+    coll_ns = sum(e - s_ for s_, e in spans)
+    inside = sum(overlap(sp, gm) for sp in spans for gm in gemms)
+    t0 = min([g[0] for g in gemms] + [sp[0] for sp in spans]) if spans or gemms else 0
+    t1 = max([g[1] for g in gemms] + [sp[1] for sp in spans]) if spans or gemms else 0
+    gemm_ns = sum(e - s_ for s_, e in gemms)
+    return {"gemms": len(gemms), "gemm_us": round(gemm_ns / 1e3, 1),
+            "collective_launches": len(spans), "collective_us": round(coll_ns / 1e3, 1),
+            "collective_us_inside_gemms": round(inside / 1e3, 1),
+            "overlap_fraction_of_collective_time": round(inside / coll_ns, 3) if coll_ns else None,
+            "first_to_last_us": round((t1 - t0) / 1e3, 1),
+            "per_gemm_us": [round((e - s_) / 1e3, 1) for s_, e in gemms]}
+
+
 def run_timeline(name):
     """A few calls of one workload on a library built with DT_TIMELINE=1, and
     the per-launch summary of their block timeline (one JSON line)."""
@@ -1173,6 +1246,22 @@ def run_timeline(name):
             dt.dt_barrier(g)
             dt.dt_all_gather(g, ALL, rs, ag, None, R // P, C * 2)
         what = "RS(avg)+AG step with barriers, P=4, bf16 [8192, 4096]: the third of 3 steps"
+    elif name == "hsdp":
+        h = HsdpSchedule(dt, dev)
+        h.mark = lambda stream, tag: dt.dt_timeline_mark(stream, tag)
+        call = h.pipelined
+        what = ("pipelined post_backward schedule, 2 x 2 mesh, 8 modules, a bf16 GEMM standing in "
+                "for each module's backward: the third of 3 runs")
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        dt.dt_timeline_start(1 << 20)
+        call()
+        rec, n = dt.dt_timeline_read(1 << 20)
+        ok = h.close()
+        print(json.dumps({"timeline": name, "what": what, "records": n, "status_ok": ok,
+                          **summarize_overlap(rec, dt)}))
+        return 0 if ok else 1
     else:
         raise ValueError(name)
     for _ in range(2):
@@ -1462,7 +1551,7 @@ def main(argv=None):
                     help="measure one collective at its own workload and print it")
     ap.add_argument("--ncu-case", choices=sorted(NCU_CASES),
                     help="run a few calls of one collective for an ncu capture (no timing)")
-    ap.add_argument("--timeline", choices=["bucket", "step"],
+    ap.add_argument("--timeline", choices=["bucket", "step", "hsdp"],
                     help="per-block kernel timeline of one call (a DT_TIMELINE=1 build)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -379,6 +379,7 @@ dt_status dt_debug_barrier_expect(dt_group_t g, int extra, uint32_t timeout_ms, 
 #define DT_TL_BUCKET 7          /* bucket all-reduce, data block */
 #define DT_TL_BUCKET_BARRIER 8  /* bucket all-reduce, the barrier block after a bucket */
 #define DT_TL_BARRIER 9         /* signal-window barrier kernel */
+#define DT_TL_MARK 10           /* dt_timeline_mark: block = the caller's tag */
 typedef struct {
     uint64_t grid;       /* the launch's %gridid */
     uint32_t kind;       /* DT_TL_* */
@@ -389,6 +390,10 @@ typedef struct {
 } dt_timeline_record;
 dt_status dt_timeline_start(size_t max_records);
 dt_status dt_timeline_read(dt_timeline_record *out, size_t max_records, size_t *n_records);
+/* A mark on the timeline at this point of `stream`: a one-thread kernel
+ * records DT_TL_MARK with block = tag, so a caller can bracket its own work
+ * (a GEMM, a copy) and compare it with the collectives' blocks. */
+dt_status dt_timeline_mark(void *stream, uint32_t tag);
 
 #ifdef __cplusplus
 }

@@ -131,9 +131,40 @@ __global__ void __launch_bounds__(kThreads) ring_kernel(const __grid_constant__ 
     if (ok) copy_bytes(p.out[r], p.stage[(r + 1) % p.bar.P], p.bytes);
 }
 
+#ifdef DT_TIMELINE
+// dt_timeline_mark: one thread records a mark carrying the caller's tag
+__global__ void mark_kernel(uint32_t tag)
+{
+    const uint64_t t = global_ns();
+    const TimelineSink s = g_timeline;
+    if (!s.rec) return;
+    const unsigned long long k = atomicAdd(s.count, 1ull);
+    if (k >= s.cap) return;
+    uint64_t grid;
+    uint32_t sm;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(grid));
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    dt_timeline_record r;
+    r.grid = grid;
+    r.kind = DT_TL_MARK;
+    r.block = tag;
+    r.sm = sm;
+    r.pad = 0;
+    r.t_start = r.t_waited = r.t_end = t;
+    s.rec[k] = r;
+}
+#endif
+
 }  // namespace
 
 DT_TL_BINDER(bind_timeline_barrier)
+
+#ifdef DT_TIMELINE
+cudaError_t launch_timeline_mark(uint32_t tag, cudaStream_t s)
+{
+    return launch_kernel(mark_kernel, dim3(1), dim3(1), 0, s, false, tag);
+}
+#endif
 
 cudaError_t launch_barrier(const BarrierParams &p, cudaStream_t s)
 {

@@ -1499,6 +1499,17 @@ dt_status dt_timeline_start(size_t max_records)
 #endif
 }
 
+dt_status dt_timeline_mark(void *stream, uint32_t tag)
+{
+#ifdef DT_TIMELINE
+    return cuda_status(dt::launch_timeline_mark(tag, static_cast<cudaStream_t>(stream)));
+#else
+    (void)stream;
+    (void)tag;
+    return DT_ERR_UNSUPPORTED;
+#endif
+}
+
 dt_status dt_timeline_read(dt_timeline_record *out, size_t max_records, size_t *n_records)
 {
 #ifdef DT_TIMELINE

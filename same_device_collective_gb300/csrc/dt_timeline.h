@@ -4,6 +4,8 @@
 // dt_timeline.cuh.  Not part of the C ABI.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include "dt.h"
 
 namespace dt {
@@ -21,6 +23,7 @@ void bind_timeline_reduce_shift(const void *sink);
 void bind_timeline_copy(const void *sink);
 void bind_timeline_bucket(const void *sink);
 void bind_timeline_barrier(const void *sink);
+cudaError_t launch_timeline_mark(uint32_t tag, cudaStream_t s);
 
 #endif
 

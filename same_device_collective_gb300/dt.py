@@ -81,6 +81,7 @@ _SIGS = {
     "dt_debug_barrier_expect": ([_vp, _i, _u32, _vp], _i),
     "dt_timeline_start": ([_sz], _i),
     "dt_timeline_read": ([_vp, _sz, _szp], _i),
+    "dt_timeline_mark": ([_vp, _u32], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -93,7 +94,7 @@ TIMELINE_DTYPE = np.dtype([("grid", np.uint64), ("kind", np.uint32), ("block", n
                            ("sm", np.uint32), ("pad", np.uint32), ("t_start", np.uint64),
                            ("t_waited", np.uint64), ("t_end", np.uint64)])
 TIMELINE_KINDS = {1: "reduce", 2: "reduce_shift", 3: "copy_bulk", 4: "copy_vec", 5: "copy_shift",
-                  6: "copy_2d", 7: "bucket", 8: "bucket_barrier", 9: "barrier"}
+                  6: "copy_2d", 7: "bucket", 8: "bucket_barrier", 9: "barrier", 10: "mark"}
 
 
 class DtError(RuntimeError):
@@ -206,6 +207,11 @@ def dt_timeline_start(max_records: int) -> None:
     """Start recording the kernel timeline (a DT_TIMELINE=1 build; raises
     DtError DT_ERR_UNSUPPORTED otherwise)."""
     _check(_lib.dt_timeline_start(max_records), "dt_timeline_start")
+
+
+def dt_timeline_mark(stream=None, tag: int = 0) -> None:
+    """A mark on the timeline at this point of the stream (DT_TIMELINE=1 builds)."""
+    _check(_lib.dt_timeline_mark(_stream(stream), tag), "dt_timeline_mark")
 
 
 def dt_timeline_read(max_records: int):

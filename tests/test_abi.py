@@ -146,6 +146,7 @@ def test_timeline_is_unsupported_in_the_default_build(dt):
     assert lib.dt_timeline_start(16) == dt.DT_ERR_UNSUPPORTED
     n = ctypes.c_size_t()
     assert lib.dt_timeline_read(None, 0, ctypes.byref(n)) == dt.DT_ERR_UNSUPPORTED
+    assert lib.dt_timeline_mark(None, 3) == dt.DT_ERR_UNSUPPORTED
     assert dt.TIMELINE_DTYPE.itemsize == 48
 
 
