@@ -395,6 +395,44 @@ dt_status dt_timeline_read(dt_timeline_record *out, size_t max_records, size_t *
  * (a GEMM, a copy) and compare it with the collectives' blocks. */
 dt_status dt_timeline_mark(void *stream, uint32_t tag);
 
+/* ------------------------------------------------------- build flavours */
+
+/* Which instrumented flavour this library is (a bit set; 0 = the default
+ * build).  Each flavour is chosen by a variable in the environment of the
+ * build and compiled into its own objects.
+ *   DT_BUILD_NVTX      every entry point opens an NVTX range (DT_NVTX=1)
+ *   DT_BUILD_TIMELINE  the kernel timeline above is recorded (DT_TIMELINE=1)
+ *   DT_BUILD_BOUNDS    bounds-checked kernels (DT_BOUNDS=1): every global
+ *                      load and store of the data kernels is checked against
+ *                      the extent of its buffer as the call's arguments give
+ *                      it.  An access outside is skipped and DT_ERR_INVALID
+ *                      is recorded in the group's error word, with
+ *                      dt_group_error_detail giving rank = the kernel
+ *                      (DT_BOUNDS_* below), peer = the buffer (reductions:
+ *                      input r as r, output q as 16 + q; copies: source
+ *                      segment s as s, destination q as 256 + q; bucket
+ *                      kernel: the tensor's index in its bucket) and
+ *                      generation = the low 31 bits of the byte offset from
+ *                      the buffer's start.  dt_bucket_allreduce_static
+ *                      has no error word: its out-of-bounds accesses are only
+ *                      skipped.  The checks cost time: for testing only.
+ *                      DT_BOUNDS_TRIM=<bytes> in the environment of a
+ *                      program using this flavour records every destination
+ *                      extent that many bytes short (a self-test of the
+ *                      checker: the stores it skips lie inside the buffers). */
+#define DT_BUILD_NVTX 1u
+#define DT_BUILD_TIMELINE 2u
+#define DT_BUILD_BOUNDS 4u
+#define DT_BOUNDS_REDUCE 1       /* AllReduce / ReduceScatter */
+#define DT_BOUNDS_REDUCE_SHIFT 2 /* the same, inputs at their own offsets */
+#define DT_BOUNDS_COPY_BULK 3
+#define DT_BOUNDS_COPY_VEC 4
+#define DT_BOUNDS_COPY_EDGE 5
+#define DT_BOUNDS_COPY_SHIFT 6
+#define DT_BOUNDS_COPY_2D 7
+#define DT_BOUNDS_BUCKET 8
+uint32_t dt_build_flags(void);
+
 #ifdef __cplusplus
 }
 #endif

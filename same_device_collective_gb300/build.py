@@ -24,7 +24,7 @@ STEP_TOOL = os.path.join(PKG, "rank_local_step")
 SOURCES = ["dt_group.cpp", "dt_reduce.cu", "dt_reduce_shift.cu", "dt_copy.cu", "dt_bucket.cu",
            "dt_barrier.cu", "dt_static.cu"]
 HEADERS = ["dt_internal.h", "dt_group.h", "dt_math.cuh", "dt_device.cuh", "dt_shift.cuh",
-           "dt_reduce_shift.h", "dt_timeline.cuh", "dt_timeline.h"]
+           "dt_reduce_shift.h", "dt_timeline.cuh", "dt_timeline.h", "dt_bounds.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the reductions use
@@ -41,6 +41,12 @@ if os.environ.get("DT_NVTX") == "1":
 if os.environ.get("DT_TIMELINE") == "1":
     NVFLAGS.append("-DDT_TIMELINE")
     BUILD = BUILD + "_timeline"
+# DT_BOUNDS=1: every data kernel checks each global load and store against the
+# extent of its buffer (from the call's arguments); an access outside records
+# DT_ERR_INVALID in the group's error word and is skipped.  Own object folder.
+if os.environ.get("DT_BOUNDS") == "1":
+    NVFLAGS.append("-DDT_BOUNDS")
+    BUILD = BUILD + "_bounds"
 
 
 def nvcc() -> str:

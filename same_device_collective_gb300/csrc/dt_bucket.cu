@@ -15,6 +15,7 @@
 #include "dt_device.cuh"
 #include "dt_math.cuh"
 #include "dt_timeline.cuh"
+#include "dt_bounds.cuh"
 
 namespace dt {
 namespace {
@@ -164,8 +165,17 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                         const uint64_t v = base + (uint64_t)u * kBucketThreads;
                         if (v < ve) {
 #pragma unroll
-                            for (int r = 0; r < PMAX; ++r)
-                                if (r < P) x[u][r] = __ldcs(static_cast<const uint4 *>(sp[r]) + v);
+                            for (int r = 0; r < PMAX; ++r) {
+                                if (r < P) {
+                                    const uint4 *a = static_cast<const uint4 *>(sp[r]) + v;
+                                    if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
+                                                             reinterpret_cast<uint64_t>(sp[r]) +
+                                                                 bt.count * (16 / EPV)),
+                                                     p.sink, kBoundsBucket, (int)t, a,
+                                                     reinterpret_cast<uint64_t>(sp[r])))
+                                        x[u][r] = __ldcs(a);
+                                }
+                            }
                         }
                     }
 #pragma unroll
@@ -174,15 +184,25 @@ bucket_kernel(const __grid_constant__ BucketParams p)
                         if (v < ve) {
                             const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
 #pragma unroll
-                            for (int r = 0; r < PMAX; ++r)
-                                if (r < P) __stcs(static_cast<uint4 *>(sp[r]) + v, y);
+                            for (int r = 0; r < PMAX; ++r) {
+                                if (r < P) {
+                                    uint4 *a = static_cast<uint4 *>(sp[r]) + v;
+                                    if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
+                                                             reinterpret_cast<uint64_t>(sp[r]) +
+                                                                 bt.count * (16 / EPV)),
+                                                     p.sink, kBoundsBucket, (int)t, a,
+                                                     reinterpret_cast<uint64_t>(sp[r])))
+                                        __stcs(a, y);
+                                }
+                            }
                         }
                     }
                 }
                 scalar_from = ve * EPV;   // ragged end of the tensor, if it is in this slice
             }
             for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kBucketThreads)
-                reduce_elem<DT, OP>(sp, 0, (int64_t)i, P, sp, P, p.avg_scale, p.avg_pow2);
+                if (DT_IN_BOUNDS(i < bt.count, p.sink, kBoundsBucket, (int)t, (const void *)(uintptr_t)i, 0))
+                    reduce_elem<DT, OP>(sp, 0, (int64_t)i, P, sp, P, p.avg_scale, p.avg_pow2);
         }
         if (++t >= p.ntensors) break;
         bt = p.tensors[t];

@@ -25,6 +25,7 @@
 #include "dt_device.cuh"
 #include "dt_shift.cuh"
 #include "dt_timeline.cuh"
+#include "dt_bounds.cuh"
 
 namespace dt {
 namespace {
@@ -60,7 +61,13 @@ copy_edge_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         for (uint32_t i = threadIdx.x; i < e * (uint32_t)sg.dst_count; i += kThreads) {
             const uint32_t k = i / e, b = i - k * e;
             const int64_t off = b < h ? (int64_t)b - (int64_t)h : (int64_t)(sg.bytes + (b - h));
-            static_cast<unsigned char *>(p.out[sg.dst_first + k])[(int64_t)sg.dst_off + off] = sg.src[off];
+            const int d = sg.dst_first + (int)k;
+            unsigned char *to = static_cast<unsigned char *>(p.out[d]) + (int64_t)sg.dst_off + off;
+            if (DT_IN_BOUNDS(span_in(sg.src + off, 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyEdge, s,
+                             sg.src + off, sg.src_lo) &&
+                DT_IN_BOUNDS(span_in(to, 1, p.out_lo[d], p.out_hi[d]), p.sink, kBoundsCopyEdge,
+                             kMaxSeg + d, to, p.out_lo[d]))
+                *to = sg.src[off];
         }
     }
 }
@@ -168,8 +175,13 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
         const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
         const int k = (int)(i % kBulkStages);
-        mbar_expect_tx(bar0 + 8 * k, nb);
-        bulk_load(buf0 + k * kBulkTile, sg.src + t0, nb, bar0 + 8 * k);
+        if (DT_IN_BOUNDS(span_in(sg.src + t0, nb, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyBulk,
+                         (int)(&sg - p.seg), sg.src + t0, sg.src_lo)) {
+            mbar_expect_tx(bar0 + 8 * k, nb);
+            bulk_load(buf0 + k * kBulkTile, sg.src + t0, nb, bar0 + 8 * k);
+        } else {
+            mbar_expect_tx(bar0 + 8 * k, 0);   // recorded and skipped: the stage completes empty
+        }
     };
 
     const uint64_t pre = n < (uint64_t)kBulkStages ? n : (uint64_t)kBulkStages;
@@ -190,9 +202,13 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         const CopySeg &sg = p.seg[find_seg(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
         const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
-        for (int d = 0; d < sg.dst_count; ++d)
-            bulk_store_hint(static_cast<unsigned char *>(p.out[sg.dst_first + d]) + sg.dst_off + t0,
-                            buf0 + k * kBulkTile, nb, pol);
+        for (int d = 0; d < sg.dst_count; ++d) {
+            const int q = sg.dst_first + d;
+            unsigned char *to = static_cast<unsigned char *>(p.out[q]) + sg.dst_off + t0;
+            if (DT_IN_BOUNDS(span_in(to, nb, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsCopyBulk, kMaxSeg + q,
+                             to, p.out_lo[q]))
+                bulk_store_hint(to, buf0 + k * kBulkTile, nb, pol);
+        }
         bulk_commit();
         // refill the stage of tile i-1 once its stores have read it
         if (i >= 1 && issued < n) {
@@ -251,10 +267,19 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         const uint64_t nch = (n - dh) / 16;
         for (int k = 0; k < nk; ++k) {
             unsigned char *D = outs[k] + sg.dst_off;
-            if (t == 0)
-                for (uint64_t b = threadIdx.x; b < dh; b += kThreads) D[b] = S[b];
-            if (t == tpp - 1)
-                for (uint64_t b = dh + nch * 16 + threadIdx.x; b < n; b += kThreads) D[b] = S[b];
+            const int q = sg.dst_first + k0 + k;
+            for (uint64_t b = threadIdx.x; t == 0 && b < dh; b += kThreads)
+                if (DT_IN_BOUNDS(span_in(S + b, 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyShift,
+                                 (int)(&sg - p.seg), S + b, sg.src_lo) &&
+                    DT_IN_BOUNDS(span_in(D + b, 1, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsCopyShift,
+                                 kMaxSeg + q, D + b, p.out_lo[q]))
+                    D[b] = S[b];
+            for (uint64_t b = dh + nch * 16 + threadIdx.x; t == tpp - 1 && b < n; b += kThreads)
+                if (DT_IN_BOUNDS(span_in(S + b, 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyShift,
+                                 (int)(&sg - p.seg), S + b, sg.src_lo) &&
+                    DT_IN_BOUNDS(span_in(D + b, 1, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsCopyShift,
+                                 kMaxSeg + q, D + b, p.out_lo[q]))
+                    D[b] = S[b];
         }
         const uint64_t c0 = t * kShiftChunks;
         const uint64_t c1 = c0 + kShiftChunks < nch ? c0 + kShiftChunks : nch;
@@ -269,13 +294,24 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
             // vector c is read for chunk c (c < c1) and, when sh > 0, for
             // chunk c - 1 (c <= c1): both hold bytes of the source
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (c < c1 || (sh && c == c1)) w = __ldcs(A + c);
+            if ((c < c1 || (sh && c == c1)) &&
+                DT_IN_BOUNDS(vector_touches(A + c, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyShift,
+                             (int)(&sg - p.seg), A + c, sg.src_lo))
+                w = __ldcs(A + c);
             uint4 nx = shfl_down_uint4(w);
-            if (lane == 31 && sh && c < c1) nx = __ldcs(A + c + 1);
+            if (lane == 31 && sh && c < c1 &&
+                DT_IN_BOUNDS(vector_touches(A + c + 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyShift,
+                             (int)(&sg - p.seg), A + c + 1, sg.src_lo))
+                nx = __ldcs(A + c + 1);
             if (c < c1) {
                 const uint4 v = sh ? shift_pair(w, nx, sh) : w;
-                for (int k = 0; k < nk; ++k)
-                    __stcs(reinterpret_cast<uint4 *>(outs[k] + sg.dst_off + dh) + c, v);
+                for (int k = 0; k < nk; ++k) {
+                    uint4 *to = reinterpret_cast<uint4 *>(outs[k] + sg.dst_off + dh) + c;
+                    const int q = sg.dst_first + k0 + k;
+                    if (DT_IN_BOUNDS(span_in(to, 16, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsCopyShift,
+                                     kMaxSeg + q, to, p.out_lo[q]))
+                        __stcs(to, v);
+                }
             }
         }
     }
@@ -317,15 +353,19 @@ copy_vec_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const uint64_t v = threadIdx.x + (uint64_t)u * kThreads;
-            if (v < nv) x[u] = __ldcs(src + v);
+            if (v < nv && DT_IN_BOUNDS(span_in(src + v, 16, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyVec,
+                                       (int)(&sg - p.seg), src + v, sg.src_lo))
+                x[u] = __ldcs(src + v);
         }
         for (int k = 0; k < sg.dst_count; ++k) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(p.out[sg.dst_first + k]) +
-                                                   sg.dst_off + t0);
+            const int q = sg.dst_first + k;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(p.out[q]) + sg.dst_off + t0);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const uint64_t v = threadIdx.x + (uint64_t)u * kThreads;
-                if (v < nv) __stcs(dst + v, x[u]);
+                if (v < nv && DT_IN_BOUNDS(span_in(dst + v, 16, p.out_lo[q], p.out_hi[q]), p.sink,
+                                           kBoundsCopyVec, kMaxSeg + q, dst + v, p.out_lo[q]))
+                    __stcs(dst + v, x[u]);
             }
         }
     }
@@ -372,12 +412,19 @@ uint64_t cut_tiles(CopyParams<NSEG, NOUT> &p, uint64_t tile_bytes)
 }
 
 template <int NSEG, int NOUT>
-cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
-                     const ErrorSink &sink, int device, cudaStream_t s)
+cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, const uint64_t *out_bytes,
+                     int nout, bool vec, const ErrorSink &sink, int device, cudaStream_t s)
 {
     CopyParams<NSEG, NOUT> p;
     memset(&p, 0, sizeof p);
-    for (int r = 0; r < nout && r < NOUT; ++r) p.out[r] = out[r];
+    for (int r = 0; r < nout && r < NOUT; ++r) {
+        p.out[r] = out[r];
+#ifdef DT_BOUNDS
+        p.out_lo[r] = reinterpret_cast<uint64_t>(out[r]);
+        p.out_hi[r] = trimmed_end(p.out_lo[r], out_bytes[r]);
+#endif
+    }
+    (void)out_bytes;
     p.sink = sink;
     int max_dst = 0;                    // most destinations of any segment
     int used = 0;
@@ -498,15 +545,18 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, int nout, 
 
 DT_TL_BINDER(bind_timeline_copy)
 
-cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, const uint64_t *out_bytes,
+                        int nout, bool vec,
                         const ErrorSink &sink, int device, cudaStream_t s)
 {
     if (nout > DT_MAX_RANKS) {
         if (nseg > DT_MAX_RANKS || nout > kMaxSeg) return cudaErrorInvalidValue;
-        return launch_n<DT_MAX_RANKS, kMaxSeg>(segs, nseg, out, nout, vec, sink, device, s);
+        return launch_n<DT_MAX_RANKS, kMaxSeg>(segs, nseg, out, out_bytes, nout, vec, sink, device, s);
     }
-    if (nseg <= DT_MAX_RANKS) return launch_n<DT_MAX_RANKS, DT_MAX_RANKS>(segs, nseg, out, nout, vec, sink, device, s);
-    if (nseg <= kMaxSeg) return launch_n<kMaxSeg, DT_MAX_RANKS>(segs, nseg, out, nout, vec, sink, device, s);
+    if (nseg <= DT_MAX_RANKS)
+        return launch_n<DT_MAX_RANKS, DT_MAX_RANKS>(segs, nseg, out, out_bytes, nout, vec, sink, device, s);
+    if (nseg <= kMaxSeg)
+        return launch_n<kMaxSeg, DT_MAX_RANKS>(segs, nseg, out, out_bytes, nout, vec, sink, device, s);
     return cudaErrorInvalidValue;
 }
 
@@ -533,9 +583,19 @@ __global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant_
             if (kVec) {
                 const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-                for (uint64_t v = lane; v < sg.row_bytes / 16; v += 32) __stcs(d4 + v, __ldcs(s4 + v));
+                for (uint64_t v = lane; v < sg.row_bytes / 16; v += 32)
+                    if (DT_IN_BOUNDS(span_in(s4 + v, 16, sg.src_lo, sg.src_hi), p.sink, kBoundsCopy2d,
+                                     (int)(&sg - p.seg), s4 + v, sg.src_lo) &&
+                        DT_IN_BOUNDS(span_in(d4 + v, 16, p.out_lo[sg.dst], p.out_hi[sg.dst]), p.sink,
+                                     kBoundsCopy2d, kMaxSeg + sg.dst, d4 + v, p.out_lo[sg.dst]))
+                        __stcs(d4 + v, __ldcs(s4 + v));
             } else {
-                for (uint64_t b = lane; b < sg.row_bytes; b += 32) dst[b] = src[b];
+                for (uint64_t b = lane; b < sg.row_bytes; b += 32)
+                    if (DT_IN_BOUNDS(span_in(src + b, 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopy2d,
+                                     (int)(&sg - p.seg), src + b, sg.src_lo) &&
+                        DT_IN_BOUNDS(span_in(dst + b, 1, p.out_lo[sg.dst], p.out_hi[sg.dst]), p.sink,
+                                     kBoundsCopy2d, kMaxSeg + sg.dst, dst + b, p.out_lo[sg.dst]))
+                        dst[b] = src[b];
             }
         }
     }
@@ -544,13 +604,24 @@ __global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant_
 
 }  // namespace
 
-cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, bool vec, int device,
-                          cudaStream_t s)
+cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, const uint64_t *out_bytes,
+                          bool vec, const ErrorSink &sink, int device, cudaStream_t s)
 {
     if (nseg > DT_MAX_RANKS * DT_MAX_RANKS) return cudaErrorInvalidValue;
     Copy2dParams p;
     memset(&p, 0, sizeof p);
-    for (int r = 0; r < DT_MAX_RANKS; ++r) p.out[r] = out[r];
+    for (int r = 0; r < DT_MAX_RANKS; ++r) {
+        p.out[r] = out[r];
+#ifdef DT_BOUNDS
+        p.out_lo[r] = reinterpret_cast<uint64_t>(out[r]);
+        p.out_hi[r] = trimmed_end(p.out_lo[r], out_bytes[r]);
+#endif
+    }
+#ifdef DT_BOUNDS
+    p.sink = sink;
+#endif
+    (void)out_bytes;
+    (void)sink;
     uint64_t tiles = 0;
     int used = 0;
     for (int i = 0; i < nseg; ++i) {

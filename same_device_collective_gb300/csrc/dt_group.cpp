@@ -701,6 +701,7 @@ dt_status dt_allreduce(dt_group_t g, int rank, const void *const *in, void *cons
     p.head = vec ? (uint32_t)head : 0;
     p.n = count - p.head;
     p.job_stride = 0;
+    dt::set_reduce_bounds(p, in, bytes, out, bytes, P, nout, error_sink(g));
     p.P = P;
     p.out_per_job = nout;
     set_avg(P, &p.avg_scale, &p.avg_pow2);
@@ -776,6 +777,7 @@ dt_status dt_reduce_scatter(dt_group_t g, int rank, const void *const *in, void 
     p.head = vec ? (uint32_t)head : 0;
     p.n = recv_count - p.head;
     p.job_stride = recv_count;
+    dt::set_reduce_bounds(p, in, in_bytes, out, out_bytes, P, P, error_sink(g));
     p.P = P;
     p.out_per_job = 1;
     set_avg(P, &p.avg_scale, &p.avg_pow2);
@@ -850,17 +852,20 @@ dt_status dt_all_gather(dt_group_t g, int rank, const void *const *in, void *con
         segs[r].tile_begin = 0;
         segs[r].dst_first = 0;
         segs[r].dst_count = (int16_t)nout;
+        dt::set_src_bounds(segs[r], in[r], segs[r].bytes);
         if (segs[r].bytes)
             vec = vec && aligned16(in[r]) && segs[r].bytes % 16 == 0 && segs[r].dst_off % 16 == 0;
     }
     void *outs[DT_MAX_RANKS] = {};
+    uint64_t ob[DT_MAX_RANKS] = {};
     for (int q = 0; q < nout; ++q) {
         outs[q] = out[q];
+        ob[q] = out_bytes;
         vec = vec && aligned16(out[q]);
     }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs, P, outs, nout, vec, error_sink(g), g->device,
+    return cuda_status(dt::launch_copy(segs, P, outs, ob, nout, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -910,13 +915,18 @@ dt_status dt_all_to_all(dt_group_t g, int rank, const void *const *in, void *con
             sg.tile_begin = 0;
             sg.dst_first = (int16_t)j;
             sg.dst_count = 1;
+            dt::set_src_bounds(sg, in[i], bytes);
         }
     }
     void *outs[DT_MAX_RANKS] = {};
-    for (int q = 0; q < P; ++q) outs[q] = out[q];
+    uint64_t ob[DT_MAX_RANKS] = {};
+    for (int q = 0; q < P; ++q) {
+        outs[q] = out[q];
+        ob[q] = bytes;
+    }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, P, vec, error_sink(g), g->device,
+    return cuda_status(dt::launch_copy(segs.data(), P * P, outs, ob, P, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -1145,6 +1155,7 @@ dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, v
     }
     dt::CopySeg segs[DT_MAX_RANKS] = {};
     void *outs[DT_MAX_RANKS] = {};
+    uint64_t ob[DT_MAX_RANKS] = {};
     bool vec = block % 16 == 0;
     for (int r = 0; r < P; ++r) {
         segs[r].src = static_cast<const unsigned char *>(in[r]) + (size_t)sidx[r] * block;
@@ -1153,12 +1164,14 @@ dt_status dt_replicate_to_shard(dt_group_t g, int rank, const void *const *in, v
         segs[r].tile_begin = 0;
         segs[r].dst_first = (int16_t)r;
         segs[r].dst_count = 1;
+        dt::set_src_bounds(segs[r], in[r], whole);
         outs[r] = out[r];
+        ob[r] = block;
         vec = vec && aligned16(in[r]) && aligned16(out[r]);
     }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs, P, outs, P, vec, error_sink(g), g->device,
+    return cuda_status(dt::launch_copy(segs, P, outs, ob, P, vec, error_sink(g), g->device,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -1211,6 +1224,7 @@ dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, 
     // stored by source (outs[r * P + q]) so a segment's destinations are adjacent
     dt::CopySeg segs[DT_MAX_RANKS] = {};
     std::vector<void *> outs((size_t)P * P);
+    std::vector<uint64_t> ob((size_t)P * P);
     bool vec = true;
     for (int r = 0; r < P; ++r) {
         segs[r].src = static_cast<const unsigned char *>(in[r]);
@@ -1219,16 +1233,18 @@ dt_status dt_all_gather_into_vec(dt_group_t g, int rank, const void *const *in, 
         segs[r].tile_begin = 0;
         segs[r].dst_first = (int16_t)(r * P);
         segs[r].dst_count = (int16_t)P;
+        dt::set_src_bounds(segs[r], in[r], nb[r]);
         if (nb[r]) vec = vec && aligned16(in[r]) && nb[r] % 16 == 0;
         for (int q = 0; q < P; ++q) {
             outs[(size_t)r * P + q] = out[q * P + r];
+            ob[(size_t)r * P + q] = nb[r];
             if (nb[r]) vec = vec && aligned16(out[q * P + r]);
         }
     }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy(segs, P, outs.data(), P * P, vec, error_sink(g), g->device,
-                                       static_cast<cudaStream_t>(stream)));
+    return cuda_status(dt::launch_copy(segs, P, outs.data(), ob.data(), P * P, vec, error_sink(g),
+                                       g->device, static_cast<cudaStream_t>(stream)));
 }
 
 dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *const *out,
@@ -1293,13 +1309,18 @@ dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *
             sg.dst_pitch = out_w * es;
             sg.rows = h;
             sg.row_bytes = w * es;
+            dt::set_src_bounds(sg, in[i], bytes);
         }
     }
     void *outs[DT_MAX_RANKS] = {};
-    for (int q = 0; q < P; ++q) outs[q] = out[q];
+    uint64_t ob[DT_MAX_RANKS] = {};
+    for (int q = 0; q < P; ++q) {
+        outs[q] = out[q];
+        ob[q] = bytes;
+    }
     DeviceScope scope(g->device);
     if (!scope.ok) return DT_ERR_CUDA;
-    return cuda_status(dt::launch_copy2d(segs.data(), P * P, outs, vec, g->device,
+    return cuda_status(dt::launch_copy2d(segs.data(), P * P, outs, ob, vec, error_sink(g), g->device,
                                          static_cast<cudaStream_t>(stream)));
 }
 
@@ -1497,6 +1518,21 @@ dt_status dt_timeline_start(size_t max_records)
     (void)max_records;
     return DT_ERR_UNSUPPORTED;
 #endif
+}
+
+uint32_t dt_build_flags(void)
+{
+    uint32_t f = 0;
+#ifdef DT_NVTX
+    f |= DT_BUILD_NVTX;
+#endif
+#ifdef DT_TIMELINE
+    f |= DT_BUILD_TIMELINE;
+#endif
+#ifdef DT_BOUNDS
+    f |= DT_BUILD_BOUNDS;
+#endif
+    return f;
 }
 
 dt_status dt_timeline_mark(void *stream, uint32_t tag)

@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <utility>
 
 #include "dt.h"
@@ -53,6 +54,12 @@ struct ReduceParams {
     int32_t out_per_job;
     uint32_t head;       // elements before the pointers above, 0..15
     uint32_t pad;
+#ifdef DT_BOUNDS
+    // each input and output buffer as the call's arguments give it
+    uint64_t in_lo[DT_MAX_RANKS], in_hi[DT_MAX_RANKS];
+    uint64_t out_lo[DT_MAX_RANKS], out_hi[DT_MAX_RANKS];
+    ErrorSink sink;
+#endif
 };
 
 // ---- byte copies (AllGather, AllToAll) ------------------------------------
@@ -76,14 +83,77 @@ struct CopySeg {
     uint8_t tail;         // < 16
     uint16_t one_pass;    // shifting copy: the destinations share their offset past a
                           // 16-byte boundary, so one pass over the source serves them all
+#ifdef DT_BOUNDS
+    uint64_t src_lo, src_hi;   // the source buffer the segment lies in
+#endif
 };
+#ifndef DT_BOUNDS
 // 40 bytes: an AllToAll's 256 entries take 10 KiB of the kernel's parameter
 // block.
 static_assert(sizeof(CopySeg) == 40, "segment entries stay 40 bytes");
+#endif
+
+#ifdef DT_BOUNDS
+// DT_BOUNDS_TRIM=<bytes> in the environment (bounds-checked builds only):
+// every destination extent is recorded that many bytes shorter than the call
+// gives it.  The kernels then skip stores that lie inside the real buffers
+// and report them, which shows the checker at work on correct kernels.
+inline uint64_t bounds_trim()
+{
+    static const uint64_t trim = [] {
+        const char *e = getenv("DT_BOUNDS_TRIM");
+        return e ? (uint64_t)strtoull(e, nullptr, 10) : 0ull;
+    }();
+    return trim;
+}
+
+inline uint64_t trimmed_end(uint64_t lo, uint64_t bytes)
+{
+    const uint64_t t = bounds_trim();
+    return lo + (bytes > t ? bytes - t : 0);
+}
+#endif
+
+// The buffers a reduction reads and writes, as the call's arguments give
+// them (checked in DT_BOUNDS builds only).
+inline void set_reduce_bounds(ReduceParams &p, const void *const *in, uint64_t in_bytes,
+                              void *const *out, uint64_t out_bytes, int nin, int nout,
+                              const ErrorSink &sink)
+{
+#ifdef DT_BOUNDS
+    for (int r = 0; r < nin; ++r) {
+        p.in_lo[r] = reinterpret_cast<uint64_t>(in[r]);
+        p.in_hi[r] = p.in_lo[r] + in_bytes;
+    }
+    for (int q = 0; q < nout; ++q) {
+        p.out_lo[q] = reinterpret_cast<uint64_t>(out[q]);
+        p.out_hi[q] = trimmed_end(p.out_lo[q], out_bytes);
+    }
+    p.sink = sink;
+#else
+    (void)p; (void)in; (void)in_bytes; (void)out; (void)out_bytes; (void)nin; (void)nout; (void)sink;
+#endif
+}
+
+// The source buffer a segment lies in (checked in DT_BOUNDS builds only).
+inline void set_src_bounds(CopySeg &sg, const void *lo, uint64_t bytes)
+{
+#ifdef DT_BOUNDS
+    sg.src_lo = reinterpret_cast<uint64_t>(lo);
+    sg.src_hi = sg.src_lo + bytes;
+#else
+    (void)sg;
+    (void)lo;
+    (void)bytes;
+#endif
+}
 
 template <int NSEG, int NOUT = DT_MAX_RANKS>
 struct CopyParams {
     void *out[NOUT];
+#ifdef DT_BOUNDS
+    uint64_t out_lo[NOUT], out_hi[NOUT];   // each destination buffer
+#endif
     ErrorSink sink;
     uint64_t tile_bytes;
     uint64_t total_tiles;
@@ -106,10 +176,29 @@ struct Copy2dSeg {
     uint64_t tile_begin;
     int32_t dst;
     int32_t pad;
+#ifdef DT_BOUNDS
+    uint64_t src_lo, src_hi;   // the source buffer the segment lies in
+#endif
 };
+
+inline void set_src_bounds(Copy2dSeg &sg, const void *lo, uint64_t bytes)
+{
+#ifdef DT_BOUNDS
+    sg.src_lo = reinterpret_cast<uint64_t>(lo);
+    sg.src_hi = sg.src_lo + bytes;
+#else
+    (void)sg;
+    (void)lo;
+    (void)bytes;
+#endif
+}
 
 struct Copy2dParams {
     void *out[DT_MAX_RANKS];
+#ifdef DT_BOUNDS
+    uint64_t out_lo[DT_MAX_RANKS], out_hi[DT_MAX_RANKS];
+    ErrorSink sink;
+#endif
     uint64_t total_tiles;
     int32_t nseg;
     int32_t pad;
@@ -234,10 +323,11 @@ cudaError_t launch_reduce(const ReduceParams &p, int dtype, int op, int jobs, bo
                           int device, cudaStream_t s);
 // nout destinations in `out` (up to DT_MAX_RANKS, or DT_MAX_RANKS^2 for the
 // vector form of AllGather)
-cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, int nout, bool vec,
-                        const ErrorSink &sink, int device, cudaStream_t s);
-cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, bool vec, int device,
-                          cudaStream_t s);
+// out_bytes[k]: the size of destination buffer k (checked in DT_BOUNDS builds)
+cudaError_t launch_copy(const CopySeg *segs, int nseg, void *const *out, const uint64_t *out_bytes,
+                        int nout, bool vec, const ErrorSink &sink, int device, cudaStream_t s);
+cudaError_t launch_copy2d(const Copy2dSeg *segs, int nseg, void *const *out, const uint64_t *out_bytes,
+                          bool vec, const ErrorSink &sink, int device, cudaStream_t s);
 // *launched (optional) tells whether a kernel went out: a bucket with no
 // elements launches nothing, and then runs no barrier either.
 cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, cudaStream_t s,

@@ -20,6 +20,7 @@
 #include "dt_device.cuh"
 #include "dt_math.cuh"
 #include "dt_timeline.cuh"
+#include "dt_bounds.cuh"
 
 namespace dt {
 namespace {
@@ -59,8 +60,14 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
             const uint64_t v = base + (uint64_t)u * kThreads;
             if (v < nvec) {
 #pragma unroll
-                for (int r = 0; r < PMAX; ++r)
-                    if (r < P) x[u][r] = __ldcs(static_cast<const uint4 *>(p.in[r]) + in_off + v);
+                for (int r = 0; r < PMAX; ++r) {
+                    if (r < P) {
+                        const uint4 *a = static_cast<const uint4 *>(p.in[r]) + in_off + v;
+                        if (DT_IN_BOUNDS(span_in(a, 16, p.in_lo[r], p.in_hi[r]), p.sink, kBoundsReduce, r, a,
+                                         p.in_lo[r]))
+                            x[u][r] = __ldcs(a);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -68,7 +75,13 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
             const uint64_t v = base + (uint64_t)u * kThreads;
             if (v < nvec) {
                 const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
-                for (int k = 0; k < ndst; ++k) __stcg(static_cast<uint4 *>(dst[k]) + v, y);
+                for (int k = 0; k < ndst; ++k) {
+                    uint4 *a = static_cast<uint4 *>(dst[k]) + v;
+                    const int q = j * p.out_per_job + k;
+                    if (DT_IN_BOUNDS(span_in(a, 16, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsReduce,
+                                     DT_MAX_RANKS + q, a, p.out_lo[q]))
+                        __stcg(a, y);
+                }
             }
         }
     }
@@ -78,10 +91,12 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
     if (blockIdx.x == 0) {
         const int64_t in_elem_off = (int64_t)j * (int64_t)p.job_stride;
         for (uint64_t i = nvec * EPV + threadIdx.x; i < p.n; i += kThreads)
-            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
-        if (threadIdx.x < p.head)
-            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)threadIdx.x - (int64_t)p.head, P, dst, ndst,
-                                p.avg_scale, p.avg_pow2);
+            if (DT_REDUCE_ELEM_OK(16 / EPV, p, kBoundsReduce, in_elem_off, (int64_t)i, dst, ndst, j))
+                reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+        const int64_t hi = (int64_t)threadIdx.x - (int64_t)p.head;
+        if (threadIdx.x < p.head &&
+            DT_REDUCE_ELEM_OK(16 / EPV, p, kBoundsReduce, in_elem_off, hi, dst, ndst, j))
+            reduce_elem<DT, OP>(p.in, in_elem_off, hi, P, dst, ndst, p.avg_scale, p.avg_pow2);
     }
     DT_TL_END_BLOCK(DT_TL_REDUCE);
 }
@@ -97,8 +112,10 @@ reduce_scalar_kernel(const __grid_constant__ ReduceParams p)
     void *const *dst = p.out + j * p.out_per_job;
     for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n;
          i += (uint64_t)gridDim.x * kThreads)
-        reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, p.P, dst, p.out_per_job, p.avg_scale,
-                            p.avg_pow2);
+        if (DT_REDUCE_ELEM_OK(DT == DT_BF16 ? 2 : 4, p, kBoundsReduce, in_elem_off, (int64_t)i, dst,
+                              p.out_per_job, j))
+            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, p.P, dst, p.out_per_job, p.avg_scale,
+                                p.avg_pow2);
 }
 
 using ReduceFn = void (*)(ReduceParams);

@@ -18,6 +18,7 @@
 #include "dt_reduce_shift.h"
 #include "dt_shift.cuh"
 #include "dt_timeline.cuh"
+#include "dt_bounds.cuh"
 
 namespace dt {
 namespace {
@@ -58,8 +59,11 @@ reduce_shift_kernel(const __grid_constant__ ReduceParams p)
                 const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(ip) & 15);
                 // vector c holds bytes of chunk c (c < nch) and, when sh > 0,
                 // of chunk c - 1 (c <= nch)
-                if (c < nch || (sh && c == nch))
-                    x[r] = __ldcs(reinterpret_cast<const uint4 *>(ip - sh) + c);
+                const uint4 *a = reinterpret_cast<const uint4 *>(ip - sh) + c;
+                if ((c < nch || (sh && c == nch)) &&
+                    DT_IN_BOUNDS(vector_touches(a, p.in_lo[r], p.in_hi[r]), p.sink, kBoundsReduceShift, r, a,
+                                 p.in_lo[r]))
+                    x[r] = __ldcs(a);
             }
         }
 #pragma unroll
@@ -73,17 +77,24 @@ reduce_shift_kernel(const __grid_constant__ ReduceParams p)
         }
         if (lane < kChunksPerWarp && c < nch) {
             const uint4 y = reduce_vec16<DT, OP, PMAX>(x, P, p.avg_scale, p.avg_pow2);
-            for (int k = 0; k < ndst; ++k)
-                __stcg(reinterpret_cast<uint4 *>(static_cast<unsigned char *>(dst[k]) + out_byte) + c, y);
+            for (int k = 0; k < ndst; ++k) {
+                uint4 *a = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(dst[k]) + out_byte) + c;
+                const int q = j * p.out_per_job + k;
+                if (DT_IN_BOUNDS(span_in(a, 16, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsReduceShift,
+                                 DT_MAX_RANKS + q, a, p.out_lo[q]))
+                    __stcg(a, y);
+            }
         }
     }
 
     // the elements before the outputs' boundary and after the last whole chunk
     if (blockIdx.x == 0) {
         for (uint64_t i = threadIdx.x; i < dh; i += kThreads)
-            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+            if (DT_REDUCE_ELEM_OK(ES, p, kBoundsReduceShift, in_elem_off, (int64_t)i, dst, ndst, j))
+                reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
         for (uint64_t i = dh + nch * EPV + threadIdx.x; i < p.n; i += kThreads)
-            reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
+            if (DT_REDUCE_ELEM_OK(ES, p, kBoundsReduceShift, in_elem_off, (int64_t)i, dst, ndst, j))
+                reduce_elem<DT, OP>(p.in, in_elem_off, (int64_t)i, P, dst, ndst, p.avg_scale, p.avg_pow2);
     }
     DT_TL_END_BLOCK(DT_TL_REDUCE_SHIFT);
 }

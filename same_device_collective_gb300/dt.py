@@ -36,6 +36,9 @@ DT_MAX_RANKS = 16
 DT_ALL_RANKS = -1
 DT_SHARED_OUTPUT = 0x1
 DT_DEFAULT_BUCKET_CAP_BYTES = 25 << 20
+DT_BUILD_NVTX, DT_BUILD_TIMELINE, DT_BUILD_BOUNDS = 1, 2, 4
+BOUNDS_KERNELS = {1: "reduce", 2: "reduce_shift", 3: "copy_bulk", 4: "copy_vec", 5: "copy_edge",
+                  6: "copy_shift", 7: "copy_2d", 8: "bucket"}
 
 DTYPES = {"f32": DT_F32, "bf16": DT_BF16, "i32": DT_I32}
 OPS = {"sum": DT_SUM, "avg": DT_AVG, "max": DT_MAX, "min": DT_MIN,
@@ -82,6 +85,7 @@ _SIGS = {
     "dt_timeline_start": ([_sz], _i),
     "dt_timeline_read": ([_vp, _sz, _szp], _i),
     "dt_timeline_mark": ([_vp, _u32], _i),
+    "dt_build_flags": ([], _u32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -201,6 +205,11 @@ def dt_status_string(status: int) -> str:
 
 def dt_launch_count() -> int:
     return int(_lib.dt_launch_count())
+
+
+def dt_build_flags() -> int:
+    """DT_BUILD_* bits of the loaded library's flavour (0: the default build)."""
+    return int(_lib.dt_build_flags())
 
 
 def dt_timeline_start(max_records: int) -> None:

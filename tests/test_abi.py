@@ -163,3 +163,30 @@ def test_timeline_flavour_compiles(tmp_path):
                os.path.join(b.CSRC, src), "-o", str(tmp_path / (src + ".o"))]
         res = subprocess.run(cmd, capture_output=True, text=True)
         assert res.returncode == 0, res.stderr
+
+
+def test_build_flags_name_the_flavour(dt):
+    # dt_build_flags reports the instrumented flavour: the timeline calls
+    # answer DT_ERR_UNSUPPORTED exactly when DT_BUILD_TIMELINE is clear.
+    lib = dt.library()
+    flags = dt.dt_build_flags()
+    assert flags & ~(dt.DT_BUILD_NVTX | dt.DT_BUILD_TIMELINE | dt.DT_BUILD_BOUNDS) == 0
+    n = ctypes.c_size_t()
+    unsupported = lib.dt_timeline_read(None, 0, ctypes.byref(n)) == dt.DT_ERR_UNSUPPORTED
+    assert unsupported == (not flags & dt.DT_BUILD_TIMELINE)
+
+
+def test_bounds_flavour_compiles(tmp_path):
+    # DT_BOUNDS=1 builds check every kernel access against its buffer; the
+    # host unit (extents from the arguments) and the bucket kernel unit must
+    # compile that way (scratch objects only).
+    import os
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    from same_device_collective_gb300 import build as b
+    for src, lang in (("dt_group.cpp", []), ("dt_bucket.cu", ["-x", "cu"])):
+        cmd = [b.nvcc(), *b.ARCH, "-O1", "-std=c++17", "-Xcompiler", "-fPIC", "-DDT_BOUNDS",
+               "-I", os.path.join(root, "include"), "-I", b.CSRC, *lang, "-c",
+               os.path.join(b.CSRC, src), "-o", str(tmp_path / (src + ".o"))]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
