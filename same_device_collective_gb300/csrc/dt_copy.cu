@@ -30,9 +30,19 @@
 namespace dt {
 namespace {
 
-template <typename Params>
+// The segment tile `tile` belongs to: a binary search over the segments'
+// first tiles, which costs log2(segments) dependent parameter-space loads,
+// or, in kernels built with kDivide, a division when the launcher set
+// seg_tiles (every segment has that many tiles).  The division stays out of
+// the other kernels' code altogether: even untaken, its branch slowed the
+// single-thread 12-deep AllToAll stream by 4% (8 ranks, 16 MiB-1 GiB per
+// rank), and taken by 8-10%, though the tiles and their order are the same.
+template <bool kDivide, typename Params>
 __device__ __forceinline__ int find_seg(const Params &p, uint64_t tile)
 {
+    if constexpr (kDivide) {
+        if (p.seg_tiles) return (int)((uint32_t)tile / p.seg_tiles);
+    }
     int lo = 0, hi = p.nseg - 1;      // last segment with tile_begin <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -171,7 +181,7 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 
     auto issue_load = [&](uint64_t i) {
         const uint64_t tile = first + i * step;
-        const CopySeg &sg = p.seg[find_seg(p, tile)];
+        const CopySeg &sg = p.seg[find_seg<KIND == kSplit>(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
         const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
         const int k = (int)(i % kBulkStages);
@@ -199,7 +209,7 @@ copy_bulk_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         }
         fence_async_shared();
         const uint64_t tile = first + i * step;
-        const CopySeg &sg = p.seg[find_seg(p, tile)];
+        const CopySeg &sg = p.seg[find_seg<KIND == kSplit>(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
         const uint32_t nb = (uint32_t)(sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes);
         for (int d = 0; d < sg.dst_count; ++d) {
@@ -252,7 +262,7 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     DT_TL_WAITED();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-        const CopySeg &sg = p.seg[find_seg(p, tile)];
+        const CopySeg &sg = p.seg[find_seg<false>(p, tile)];
         const uint64_t tpp = shift_tiles(sg.bytes);
         const uint64_t idx = tile - sg.tile_begin;
         // one pass for all destinations, or tiles of one destination at a time
@@ -337,7 +347,7 @@ bool use_small_copy(uint64_t src_bytes, int nseg, int max_dst)
     return src_bytes <= (16ull << 20) && src_bytes / (uint64_t)nseg >= (64ull << 10);
 }
 
-template <int NSEG, int NOUT>
+template <int NSEG, int NOUT, bool kDivide>
 __global__ void __launch_bounds__(kThreads)
 copy_vec_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
 {
@@ -345,7 +355,7 @@ copy_vec_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
     pdl_begin();
     DT_TL_WAITED();
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-        const CopySeg &sg = p.seg[find_seg(p, tile)];
+        const CopySeg &sg = p.seg[find_seg<kDivide>(p, tile)];
         const uint64_t t0 = (tile - sg.tile_begin) * p.tile_bytes;
         const uint64_t nv = (sg.bytes - t0 < p.tile_bytes ? sg.bytes - t0 : p.tile_bytes) / 16;
         const uint4 *src = reinterpret_cast<const uint4 *>(sg.src + t0);
@@ -403,11 +413,20 @@ uint64_t cut_tiles(CopyParams<NSEG, NOUT> &p, uint64_t tile_bytes)
 {
     p.tile_bytes = tile_bytes;
     uint64_t tiles = 0;
+    bool equal = true;
+    const uint64_t first = (p.seg[0].bytes + tile_bytes - 1) / tile_bytes;
     for (int i = 0; i < p.nseg; ++i) {
         p.seg[i].tile_begin = tiles;
-        tiles += (p.seg[i].bytes + tile_bytes - 1) / tile_bytes;
+        const uint64_t t = (p.seg[i].bytes + tile_bytes - 1) / tile_bytes;
+        equal = equal && t == first;
+        tiles += t;
     }
     p.total_tiles = tiles;
+    // Equal segments are found by a division from 8 segments on (AllToAlls of
+    // 8 and 16 ranks at 4-256 KiB per rank 1.22-1.45x, 1 MiB 1.18-1.24x;
+    // 8- and 16-rank gathers of up to 256 KiB 1.02-1.12x); with fewer the
+    // search is as short as the division (2-rank gathers lost 3-4%).
+    p.seg_tiles = equal && p.nseg >= 8 && first > 0 && tiles < (1ull << 32) ? (uint32_t)first : 0u;
     return tiles;
 }
 
@@ -465,6 +484,7 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, const uint
                 tiles += shift_tiles(sg.bytes) * (one ? 1 : (uint64_t)sg.dst_count);
             }
             p.total_tiles = tiles;
+            p.seg_tiles = 0;             // segments of different tile counts: search
             p.tile_bytes = kShiftTile;
             void (*fn)(CopyParams<NSEG, NOUT>) = copy_shift_kernel<NSEG, NOUT>;
             int resident = 0;
@@ -503,7 +523,8 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, const uint
     for (int i = 0; i < p.nseg; ++i) src_bytes += p.seg[i].bytes;
     if (use_small_copy(src_bytes, p.nseg, max_dst)) {
         const uint64_t tiles = cut_tiles(p, kSmallTile);
-        void (*fn)(CopyParams<NSEG, NOUT>) = copy_vec_kernel<NSEG, NOUT>;
+        void (*fn)(CopyParams<NSEG, NOUT>) =
+            p.seg_tiles ? copy_vec_kernel<NSEG, NOUT, true> : copy_vec_kernel<NSEG, NOUT, false>;
         int resident = 0;
         cudaError_t e = resident_blocks(reinterpret_cast<const void *>(fn), kThreads, device, &resident);
         if (e != cudaSuccess) return e;
@@ -532,7 +553,7 @@ cudaError_t launch_n(const CopySeg *segs, int nseg, void *const *out, const uint
         // over every SM's copy engine (8 ranks, 256 KiB per rank: the split
         // shape lost 16%)
         if ((p.nseg <= 64 && 2 * src_bytes > l2_bytes(device)) || tiles <= (uint64_t)sm_count(device))
-            return launch_bulk<NSEG, NOUT, kStream>(p, device, s);
+            return launch_bulk<NSEG, NOUT, kStream>(p, device, s);   // searches (see find_seg)
         return launch_bulk<NSEG, NOUT, kSplit>(p, device, s);
     }
     if (max_dst <= 8 && cut_tiles(p, BulkShape<kGatherSplit>::kTile) >= 3 * (uint64_t)sm_count(device))
@@ -573,7 +594,7 @@ __global__ void __launch_bounds__(kThreads) copy2d_kernel(const __grid_constant_
     DT_TL_WAITED();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (uint64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-        const Copy2dSeg &sg = p.seg[find_seg(p, tile)];
+        const Copy2dSeg &sg = p.seg[find_seg<false>(p, tile)];
         const uint64_t r0 = (tile - sg.tile_begin) * sg.rows_per_tile;
         const uint64_t r1 = r0 + sg.rows_per_tile < sg.rows ? r0 + sg.rows_per_tile : sg.rows;
         unsigned char *dbase = static_cast<unsigned char *>(p.out[sg.dst]) + sg.dst_off;

@@ -158,7 +158,8 @@ struct CopyParams {
     uint64_t tile_bytes;
     uint64_t total_tiles;
     int32_t nseg;
-    int32_t pad;
+    uint32_t seg_tiles;   // tiles of every segment when they are all equal (and fewer than 2^32
+                          // tiles in all): the segment of tile t is t / seg_tiles; else 0
     CopySeg seg[NSEG];
 };
 
@@ -201,7 +202,7 @@ struct Copy2dParams {
 #endif
     uint64_t total_tiles;
     int32_t nseg;
-    int32_t pad;
+    uint32_t seg_tiles;   // as in CopyParams
     Copy2dSeg seg[DT_MAX_RANKS * DT_MAX_RANKS];
 };
 
