@@ -277,7 +277,8 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
         const uint64_t nch = (n - dh) / 16;
         for (int k = 0; k < nk; ++k) {
             unsigned char *D = outs[k] + sg.dst_off;
-            const int q = sg.dst_first + k0 + k;
+            const int q = sg.dst_first + k0 + k;   // for the bounds checks
+            (void)q;
             for (uint64_t b = threadIdx.x; t == 0 && b < dh; b += kThreads)
                 if (DT_IN_BOUNDS(span_in(S + b, 1, sg.src_lo, sg.src_hi), p.sink, kBoundsCopyShift,
                                  (int)(&sg - p.seg), S + b, sg.src_lo) &&
@@ -317,7 +318,8 @@ copy_shift_kernel(const __grid_constant__ CopyParams<NSEG, NOUT> p)
                 const uint4 v = sh ? shift_pair(w, nx, sh) : w;
                 for (int k = 0; k < nk; ++k) {
                     uint4 *to = reinterpret_cast<uint4 *>(outs[k] + sg.dst_off + dh) + c;
-                    const int q = sg.dst_first + k0 + k;
+                    const int q = sg.dst_first + k0 + k;   // for the bounds checks
+                    (void)q;
                     if (DT_IN_BOUNDS(span_in(to, 16, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsCopyShift,
                                      kMaxSeg + q, to, p.out_lo[q]))
                         __stcs(to, v);

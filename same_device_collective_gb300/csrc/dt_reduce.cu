@@ -77,7 +77,8 @@ reduce_vec_kernel(const __grid_constant__ ReduceParams p)
                 const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
                 for (int k = 0; k < ndst; ++k) {
                     uint4 *a = static_cast<uint4 *>(dst[k]) + v;
-                    const int q = j * p.out_per_job + k;
+                    const int q = j * p.out_per_job + k;   // for the bounds checks
+                    (void)q;
                     if (DT_IN_BOUNDS(span_in(a, 16, p.out_lo[q], p.out_hi[q]), p.sink, kBoundsReduce,
                                      DT_MAX_RANKS + q, a, p.out_lo[q]))
                         __stcg(a, y);
