@@ -190,3 +190,47 @@ def test_bounds_flavour_compiles(tmp_path):
                os.path.join(b.CSRC, src), "-o", str(tmp_path / (src + ".o"))]
         res = subprocess.run(cmd, capture_output=True, text=True)
         assert res.returncode == 0, res.stderr
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dt.h"
+
+int main(void)
+{
+    dt_group_t g = 0;
+    /* calls that need no device: argument checks, strings, flags */
+    if (dt_group_create(0, 0, &g) != DT_ERR_INVALID) return 1;
+    if (dt_group_destroy(0) != DT_ERR_INVALID) return 2;
+    if (strlen(dt_status_string(DT_OK)) == 0) return 3;
+    /* 2-byte elements, 40-byte cap: 20 B | 40 B | 60 B (over the cap, alone) */
+    size_t counts[3] = {10, 20, 30}, bucket_of[3] = {9, 9, 9}, n_buckets = 0;
+    if (dt_bucket_plan(counts, 3, 2, 40, bucket_of, &n_buckets) != DT_OK) return 4;
+    if (n_buckets != 3 || bucket_of[0] != 0 || bucket_of[1] != 1 || bucket_of[2] != 2) return 5;
+    printf("%u\n", dt_build_flags());
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    # include/dt.h is a C header: a C11 program that includes it compiles
+    # with every warning an error, links against libdt.so and calls the
+    # entry points that need no device.
+    import os
+    import subprocess
+    from same_device_collective_gb300 import build as b
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    pkg = os.path.dirname(b.LIB)
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+           "-I", os.path.join(root, "include"), str(src), "-o", str(exe),
+           "-L", pkg, "-ldt", "-Wl,-rpath," + pkg]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.strip().isdigit()
