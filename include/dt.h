@@ -250,9 +250,11 @@ dt_status dt_all_to_all_2d(dt_group_t g, int rank, const void *const *in, void *
  * table (no flatten copy), and one signal-window barrier (the notify / wait
  * of dt_barrier, one generation each) runs between consecutive buckets: in an
  * extra last block of the earlier bucket's kernel, which waits until that
- * bucket's other blocks have finished.  The next bucket's kernel starts once
- * that whole kernel has completed.  The plan table is staged through the
- * group's scratch; at most one bucket call per group may be in flight. */
+ * bucket's other blocks have finished.  The next bucket's kernel stores
+ * nothing before that whole kernel has completed (its first blocks load
+ * their first gradients while it drains: tensors no kernel of the call has
+ * written yet).  The plan table is staged through the group's scratch; at
+ * most one bucket call per group may be in flight. */
 dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *counts,
                               size_t n_tensors, int dtype, int op, size_t bucket_cap_bytes,
                               void *stream);

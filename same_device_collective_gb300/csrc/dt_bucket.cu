@@ -56,6 +56,7 @@ __device__ void bucket_barrier_block(const BucketParams &p)
     // counting themselves out and whose barrier block has yet to update the
     // window.  Touch neither before it has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!p.early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         ok = 1;
         const uint32_t others = gridDim.x - 1;
@@ -122,14 +123,23 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     __shared__ void *sp[DT_MAX_RANKS];
     const int P = p.P;
-    // Let the next kernel begin launching, then fetch this block's first
-    // tensor entry and that tensor's P rank pointers before waiting for the
-    // previous kernel: the plan table is staged by a host copy that precedes
-    // the call's first kernel in stream order, and no kernel writes it.  The
-    // gradients themselves are touched only after griddepcontrol.wait.  This
-    // takes two dependent table reads off the start of every bucket.
+    // Fetch this block's first tensor entry and that tensor's P rank pointers
+    // before waiting for the previous kernel: the plan table is staged by a
+    // host copy that precedes the call's first kernel in stream order, and no
+    // kernel writes it.  This takes two dependent table reads off the start
+    // of every bucket.
+    //
+    // Every bucket kernel of a call after the first also loads its block's
+    // first vectors of gradients before the wait, so the blocks that become
+    // resident while the previous bucket drains (up to one per free slot)
+    // have their data in flight when it completes; nothing is stored before
+    // the wait, and so before the barrier between the buckets.  Those loads
+    // read this bucket's tensors, which no kernel of the call writes before
+    // this one; the call's first kernel lets the next launch begin only after
+    // its own wait, so no early load can overtake the work queued before the
+    // call.  The other kernels let the next one launch at once.
     DT_TL_BEGIN();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (p.win && blockIdx.x == gridDim.x - 1) {
         bucket_barrier_block(p);
         DT_TL_WAITED();
@@ -146,7 +156,40 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     uint32_t t = p.block_start[blockIdx.x];   // its first <= lo < hi
     BucketTensor bt = p.tensors[t];
     if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)(bt.slot & 0x7FFFFFFFu) * P + threadIdx.x];
+
+    uint4 x[U][PMAX];
+    // U vectors from every rank of tensor t at vector positions base, base +
+    // kBucketThreads, ... below ve
+    auto load_vectors = [&](uint64_t base, uint64_t ve) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = base + (uint64_t)u * kBucketThreads;
+            if (v < ve) {
+#pragma unroll
+                for (int r = 0; r < PMAX; ++r) {
+                    if (r < P) {
+                        const uint4 *a = static_cast<const uint4 *>(sp[r]) + v;
+                        if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
+                                                 reinterpret_cast<uint64_t>(sp[r]) + bt.count * (16 / EPV)),
+                                         p.sink, kBoundsBucket, (int)t, a, reinterpret_cast<uint64_t>(sp[r])))
+                            x[u][r] = __ldcs(a);
+                    }
+                }
+            }
+        }
+    };
+    bool loaded = false;   // x holds the first pass of the first tensor
+    if (p.early) {
+        __syncthreads();   // sp
+        const uint64_t s0 = (lo > bt.first ? lo : bt.first) - bt.first;
+        const uint64_t e0 = hi - bt.first < bt.count ? hi - bt.first : bt.count;
+        if ((bt.slot >> 31) && s0 < e0 && s0 / EPV + threadIdx.x < e0 / EPV) {
+            load_vectors(s0 / EPV + threadIdx.x, e0 / EPV);
+            loaded = true;
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!p.early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
     DT_TL_WAITED();
 
@@ -159,25 +202,10 @@ bucket_kernel(const __grid_constant__ BucketParams p)
             if (bt.slot >> 31) {
                 const uint64_t vs = s / EPV, ve = e / EPV;   // s is a multiple of EPV
                 for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kBucketThreads * U) {
-                    uint4 x[U][PMAX];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const uint64_t v = base + (uint64_t)u * kBucketThreads;
-                        if (v < ve) {
-#pragma unroll
-                            for (int r = 0; r < PMAX; ++r) {
-                                if (r < P) {
-                                    const uint4 *a = static_cast<const uint4 *>(sp[r]) + v;
-                                    if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
-                                                             reinterpret_cast<uint64_t>(sp[r]) +
-                                                                 bt.count * (16 / EPV)),
-                                                     p.sink, kBoundsBucket, (int)t, a,
-                                                     reinterpret_cast<uint64_t>(sp[r])))
-                                        x[u][r] = __ldcs(a);
-                                }
-                            }
-                        }
-                    }
+                    if (loaded)
+                        loaded = false;   // loaded before the wait
+                    else
+                        load_vectors(base, ve);
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const uint64_t v = base + (uint64_t)u * kBucketThreads;

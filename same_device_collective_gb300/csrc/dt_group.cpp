@@ -1090,6 +1090,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
     // The barrier between buckets b and b + 1 runs in an extra last block of
     // bucket b's kernel (the buckets' data decides nothing about it, so an
     // empty bucket still gets its barrier from a kernel of its own).
+    bool kernel_before = false;   // a bucket kernel of this call is already queued
     for (size_t b = 0; b < bl.size(); ++b) {
         const dt_group::PlanLaunch &L = bl[b];
         bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
@@ -1099,9 +1100,11 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         bp.per_block = L.per_block;
         const bool barrier_after = b + 1 < bl.size();
         bp.win = barrier_after ? g->d_win : nullptr;
+        bp.early = kernel_before ? 1u : 0u;
         bool launched = false;
         e = dt::launch_bucket(bp, dtype, op, g->device, s, &launched);
         if (e != cudaSuccess) break;
+        kernel_before = kernel_before || launched;
         if (barrier_after) {
             if (launched) {
                 g->barriers_issued++;

@@ -229,6 +229,10 @@ struct BucketParams {
     int32_t P;
     float avg_scale;
     int32_t avg_pow2;
+    // 1 in every bucket kernel of a call but the first: its blocks load their
+    // first vectors before waiting for the previous kernel (see bucket_kernel)
+    uint32_t early;
+    uint32_t pad;
     // The signal-window barrier after this bucket, run by one extra block at
     // the end of the grid (win != nullptr; see bucket_kernel): the group's
     // window [P][P], followed by rank_gen[P] and the counter of finished

@@ -122,6 +122,7 @@ dt_status launch_all(const unsigned char *d, size_t ptr_bytes, size_t tab_bytes,
     bp.P = P;
     bp.avg_pow2 = (P & (P - 1)) == 0;
     bp.avg_scale = bp.avg_pow2 ? 1.0f / (float)P : 0.0f;
+    bool kernel_before = false;   // a bucket kernel of this call is already queued
     for (size_t i = 0; i < nl; ++i) {
         const Launch &L = g_launches[i];
         bp.tensors = reinterpret_cast<const dt::BucketTensor *>(d + ptr_bytes) + L.tb;
@@ -129,7 +130,10 @@ dt_status launch_all(const unsigned char *d, size_t ptr_bytes, size_t tab_bytes,
         bp.ntensors = (uint32_t)(L.te - L.tb);
         bp.total = L.total;
         bp.per_block = L.per_block;
-        if (dt::launch_bucket(bp, dtype, op, device, s) != cudaSuccess) return DT_ERR_CUDA;
+        bp.early = kernel_before ? 1u : 0u;
+        bool launched = false;
+        if (dt::launch_bucket(bp, dtype, op, device, s, &launched) != cudaSuccess) return DT_ERR_CUDA;
+        kernel_before = kernel_before || launched;
     }
     return DT_OK;
 }
