@@ -37,14 +37,14 @@ constexpr int kBucketThreads = 128;
 // count themselves out in the group's finished-block counter as they end;
 // this block, dispatched after all of them, waits for the previous kernel,
 // then until the count is complete, resets it for the next bucket kernel, and
-// then acts for all P
-// ranks at once: thread cell (r, q) adds 1 to row r of peer q's window (rank
-// r's notify, AtomicAdd) and then waits until row q of rank r's window
-// reaches rank r's generation (Ge).  The next kernel starts after this grid
-// has completed, so it sees every gradient this bucket wrote, as it would
-// after a barrier kernel -- whose own launch-to-completion hop is what this
-// saves at every bucket boundary.  Every wait is bounded: one that runs out
-// records DT_ERR_TIMEOUT and ends the block.
+// then acts for all P ranks at once: thread cell (r, q) adds 1 to row r of
+// peer q's window (rank r's notify, AtomicAdd) and then waits until row q of
+// rank r's window reaches rank r's generation (Ge).  The next kernel stores
+// nothing before this grid has completed, so it sees every gradient this
+// bucket wrote, as it would after a barrier kernel -- whose own
+// launch-to-completion hop is what this saves at every bucket boundary.
+// Every wait is bounded: one that runs out records DT_ERR_TIMEOUT and ends
+// the block.
 __device__ void bucket_barrier_block(const BucketParams &p)
 {
     __shared__ int ok;
