@@ -6,11 +6,11 @@
 // (PyTorch communication page §六.5) gathers gradients into 25 MB buckets so
 // that one bandwidth-bound call replaces many latency-bound ones.  Here the
 // bucket is never flattened into a copy: the host hands the kernel a table of
-// the bucket's tensors (their place in the bucket's flattened element space)
-// and the P rank pointers of each, and every block reduces an equal,
-// contiguous slice of that space in place in every rank's gradient, reading
-// each element once per rank and writing it once per rank.  Equal slices keep
-// the blocks balanced however uneven the tensor sizes are.
+// the bucket's tensors and the P rank pointers of each, and every block
+// reduces one slice of one tensor in place in every rank's gradient, reading
+// each element once per rank and writing it once per rank.  The slices have
+// one length for the whole bucket (a tensor's last one is shorter), which
+// keeps the blocks balanced however uneven the tensor sizes are.
 #include "dt_internal.h"
 #include "dt_device.cuh"
 #include "dt_math.cuh"
@@ -123,14 +123,16 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     constexpr int EPV = DT == DT_BF16 ? 8 : 4;   // elements per 16-byte vector
     __shared__ void *sp[DT_MAX_RANKS];
     const int P = p.P;
-    // Fetch this block's first tensor entry and that tensor's P rank pointers
-    // before waiting for the previous kernel: the plan table is staged by a
-    // host copy that precedes the call's first kernel in stream order, and no
-    // kernel writes it.  This takes two dependent table reads off the start
-    // of every bucket.
+    // Fetch this block's tensor entry and that tensor's P rank pointers before
+    // waiting for the previous kernel: the plan table is staged by a host copy
+    // that precedes the call's first kernel in stream order, and no kernel
+    // writes it.  This takes two dependent table reads off the start of every
+    // bucket.  A block works on one tensor: blocks whose slice crossed into a
+    // second tensor took it after the first, ran 2.7x as long as the others
+    // and were the last to end in nearly every bucket.
     //
     // Every bucket kernel of a call after the first also loads its block's
-    // first vectors of gradients before the wait, so the blocks that become
+    // first pass of gradients before the wait, so the blocks that become
     // resident while the previous bucket drains (up to one per free slot)
     // have their data in flight when it completes; nothing is stored before
     // the wait, and so before the barrier between the buckets.  Those loads
@@ -146,20 +148,14 @@ bucket_kernel(const __grid_constant__ BucketParams p)
         DT_TL_END_BLOCK(DT_TL_BUCKET_BARRIER);
         return;
     }
-    const uint64_t lo = (uint64_t)blockIdx.x * p.per_block;
-    if (lo >= p.total) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        count_out(p);
-        return;
-    }
-    const uint64_t hi = lo + p.per_block < p.total ? lo + p.per_block : p.total;
-    uint32_t t = p.block_start[blockIdx.x];   // its first <= lo < hi
-    BucketTensor bt = p.tensors[t];
+    const uint32_t t = p.block_start[blockIdx.x];
+    const BucketTensor bt = p.tensors[t];
+    const uint64_t lo = (uint64_t)(blockIdx.x - bt.block0) * p.per_block;   // within the tensor
+    const uint64_t hi = lo + p.per_block < bt.count ? lo + p.per_block : bt.count;
     if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)(bt.slot & 0x7FFFFFFFu) * P + threadIdx.x];
 
     uint4 x[U][PMAX];
-    // U vectors from every rank of tensor t at vector positions base, base +
-    // kBucketThreads, ... below ve
+    // U vectors from every rank at vector positions base, base + kBucketThreads, ... below ve
     auto load_vectors = [&](uint64_t base, uint64_t ve) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -178,13 +174,14 @@ bucket_kernel(const __grid_constant__ BucketParams p)
             }
         }
     };
-    bool loaded = false;   // x holds the first pass of the first tensor
+    // the slice's whole vectors (all ranks 16-byte aligned), then its other elements
+    const bool aligned = bt.slot >> 31;
+    const uint64_t vs = lo / EPV, ve = aligned ? hi / EPV : vs;   // lo is a multiple of EPV
+    bool loaded = false;   // x holds the first pass
     if (p.early) {
         __syncthreads();   // sp
-        const uint64_t s0 = (lo > bt.first ? lo : bt.first) - bt.first;
-        const uint64_t e0 = hi - bt.first < bt.count ? hi - bt.first : bt.count;
-        if ((bt.slot >> 31) && s0 < e0 && s0 / EPV + threadIdx.x < e0 / EPV) {
-            load_vectors(s0 / EPV + threadIdx.x, e0 / EPV);
+        if (vs + threadIdx.x < ve) {
+            load_vectors(vs + threadIdx.x, ve);
             loaded = true;
         }
     }
@@ -193,52 +190,34 @@ bucket_kernel(const __grid_constant__ BucketParams p)
     __syncthreads();
     DT_TL_WAITED();
 
-    for (;;) {
-        const uint64_t s = (lo > bt.first ? lo : bt.first) - bt.first;   // local range [s, e)
-        uint64_t e = hi - bt.first;
-        if (e > bt.count) e = bt.count;
-        if (s < e) {   // else only padding of this tensor lies in the slice
-            uint64_t scalar_from = s;
-            if (bt.slot >> 31) {
-                const uint64_t vs = s / EPV, ve = e / EPV;   // s is a multiple of EPV
-                for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kBucketThreads * U) {
-                    if (loaded)
-                        loaded = false;   // loaded before the wait
-                    else
-                        load_vectors(base, ve);
+    for (uint64_t base = vs + threadIdx.x; base < ve; base += (uint64_t)kBucketThreads * U) {
+        if (loaded)
+            loaded = false;   // loaded before the wait
+        else
+            load_vectors(base, ve);
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const uint64_t v = base + (uint64_t)u * kBucketThreads;
-                        if (v < ve) {
-                            const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = base + (uint64_t)u * kBucketThreads;
+            if (v < ve) {
+                const uint4 y = reduce_vec16<DT, OP, PMAX>(x[u], P, p.avg_scale, p.avg_pow2);
 #pragma unroll
-                            for (int r = 0; r < PMAX; ++r) {
-                                if (r < P) {
-                                    uint4 *a = static_cast<uint4 *>(sp[r]) + v;
-                                    if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
-                                                             reinterpret_cast<uint64_t>(sp[r]) +
-                                                                 bt.count * (16 / EPV)),
-                                                     p.sink, kBoundsBucket, (int)t, a,
-                                                     reinterpret_cast<uint64_t>(sp[r])))
-                                        __stcs(a, y);
-                                }
-                            }
-                        }
+                for (int r = 0; r < PMAX; ++r) {
+                    if (r < P) {
+                        uint4 *a = static_cast<uint4 *>(sp[r]) + v;
+                        if (DT_IN_BOUNDS(span_in(a, 16, reinterpret_cast<uint64_t>(sp[r]),
+                                                 reinterpret_cast<uint64_t>(sp[r]) + bt.count * (16 / EPV)),
+                                         p.sink, kBoundsBucket, (int)t, a, reinterpret_cast<uint64_t>(sp[r])))
+                            __stcs(a, y);
                     }
                 }
-                scalar_from = ve * EPV;   // ragged end of the tensor, if it is in this slice
             }
-            for (uint64_t i = scalar_from + threadIdx.x; i < e; i += kBucketThreads)
-                if (DT_IN_BOUNDS(i < bt.count, p.sink, kBoundsBucket, (int)t, (const void *)(uintptr_t)i, 0))
-                    reduce_elem<DT, OP>(sp, 0, (int64_t)i, P, sp, P, p.avg_scale, p.avg_pow2);
         }
-        if (++t >= p.ntensors) break;
-        bt = p.tensors[t];
-        if (bt.first >= hi) break;
-        __syncthreads();   // every thread is done with the previous tensor's pointers
-        if (threadIdx.x < P) sp[threadIdx.x] = p.ptrs[(uint64_t)(bt.slot & 0x7FFFFFFFu) * P + threadIdx.x];
-        __syncthreads();
     }
+    // the ragged end of the tensor, if it is in this slice, or the whole slice
+    // of a tensor whose ranks are not all 16-byte aligned
+    for (uint64_t i = ve * EPV + threadIdx.x; i < hi; i += kBucketThreads)
+        if (DT_IN_BOUNDS(i < bt.count, p.sink, kBoundsBucket, (int)t, (const void *)(uintptr_t)i, 0))
+            reduce_elem<DT, OP>(sp, 0, (int64_t)i, P, sp, P, p.avg_scale, p.avg_pow2);
     count_out(p);
     DT_TL_END_BLOCK(DT_TL_BUCKET);
 }
@@ -270,6 +249,11 @@ uint64_t bucket_padded(uint64_t count, int dtype)
 {
     const uint64_t epv = dtype == DT_BF16 ? 8 : 4;
     return (count + epv - 1) / epv * epv;
+}
+
+uint64_t bucket_tensor_blocks(uint64_t count, int dtype, uint64_t per_block)
+{
+    return (bucket_padded(count, dtype) + per_block - 1) / per_block;
 }
 
 cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, uint32_t *blocks,
@@ -309,10 +293,10 @@ cudaError_t launch_bucket(const BucketParams &p, int dtype, int op, int device, 
     if (launched) *launched = false;
     BucketFn fn = pick_fn(dtype, op, p.P);
     if (!fn) return cudaErrorInvalidValue;
-    if (p.total == 0 || p.ntensors == 0) return cudaSuccess;
+    if (p.blocks == 0 || p.ntensors == 0) return cudaSuccess;
     (void)device;
     // data blocks, plus the barrier block when a barrier follows the bucket
-    const unsigned gx = (unsigned)((p.total + p.per_block - 1) / p.per_block) + (p.win ? 1u : 0u);
+    const unsigned gx = p.blocks + (p.win ? 1u : 0u);
     const cudaError_t e = launch_kernel(fn, dim3(gx), dim3(kBucketThreads), 0, s, false, p);
     if (launched) *launched = e == cudaSuccess;
     return e;

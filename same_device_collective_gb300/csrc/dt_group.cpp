@@ -1009,6 +1009,11 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
             if (L.total) {
                 e = dt::bucket_grid(dtype, op, P, L.total, g->device, &L.blocks, &L.per_block);
                 if (e != cudaSuccess) return cuda_status(e);
+                // one block per slice of a tensor: the grid's slice length, cut at tensor ends
+                uint64_t nblk = 0;
+                for (size_t u = L.tb; u < L.te; ++u) nblk += dt::bucket_tensor_blocks(counts[u], dtype, L.per_block);
+                if (nblk > UINT32_MAX / 2) return DT_ERR_INVALID;
+                L.blocks = (uint32_t)nblk;
             }
             L.start_off = n_starts;
             n_starts += L.blocks;
@@ -1042,21 +1047,17 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         uint32_t *starts = reinterpret_cast<uint32_t *>(h + ptr_bytes + tab_bytes);
         for (const dt_group::PlanLaunch &L : bl) {
             uint64_t first = 0;
+            uint32_t block = 0;   // the bucket's blocks, tensor by tensor
             for (size_t t = L.tb; t < L.te; ++t) {
                 bool al = true;
                 for (int p = 0; p < P; ++p) al = al && aligned16(grads[t * P + p]);
                 tab[t].first = first;
                 tab[t].count = counts[t];
                 tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
-                tab[t].pad = 0;
+                tab[t].block0 = block;
                 first += dt::bucket_padded(counts[t], dtype);
-            }
-            // block j starts at the last tensor (bucket-relative) with first <= j * per_block
-            size_t t = L.tb;
-            for (uint32_t j = 0; j < L.blocks; ++j) {
-                const uint64_t lo = (uint64_t)j * L.per_block;
-                while (t + 1 < L.te && tab[t + 1].first <= lo) ++t;
-                starts[L.start_off + j] = (uint32_t)(t - L.tb);
+                const uint64_t nb_t = L.total ? dt::bucket_tensor_blocks(counts[t], dtype, L.per_block) : 0;
+                for (uint64_t j = 0; j < nb_t; ++j) starts[L.start_off + block++] = (uint32_t)(t - L.tb);
             }
         }
         e = cudaMemcpyAsync(sl.d, h, plan_bytes, cudaMemcpyHostToDevice, s);
@@ -1098,6 +1099,7 @@ dt_status dt_bucket_allreduce(dt_group_t g, void *const *grads, const size_t *co
         bp.ntensors = (uint32_t)(L.te - L.tb);
         bp.total = L.total;
         bp.per_block = L.per_block;
+        bp.blocks = L.blocks;
         const bool barrier_after = b + 1 < bl.size();
         bp.win = barrier_after ? g->d_win : nullptr;
         bp.early = kernel_before ? 1u : 0u;

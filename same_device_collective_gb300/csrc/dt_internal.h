@@ -208,20 +208,21 @@ struct Copy2dParams {
 
 // ---- fused bucket all-reduce ----------------------------------------------
 // A bucket's tensors laid end to end form its flattened element space, in
-// which every tensor occupies its count rounded up to a whole 16-byte vector,
-// so that any boundary that is a multiple of the vector width is one inside
-// every tensor too.  Block b reduces the slice [b * per_block, (b + 1) *
-// per_block) of that space, starting at tensor block_start[b].
+// which every tensor occupies its count rounded up to a whole 16-byte vector.
+// Each tensor is cut into slices of per_block elements (its last slice
+// shorter), one block per slice, so that no block works on two tensors:
+// block b works on tensor block_start[b], on its elements [(b - block0) *
+// per_block, + per_block) below its count.
 struct BucketTensor {
     uint64_t first;   // first element in the bucket's flattened space
     uint64_t count;   // elements of the tensor
     uint32_t slot;    // row of P pointers in `ptrs`; bit 31: all 16-byte aligned
-    uint32_t pad;
+    uint32_t block0;  // the bucket's first block that works on this tensor
 };
 
 struct BucketParams {
     const BucketTensor *tensors;     // this bucket's tensors, in order
-    const uint32_t *block_start;     // per block: index of its first tensor
+    const uint32_t *block_start;     // per block: index of its tensor
     void *const *ptrs;               // [n_slots][P]
     uint64_t total;                  // padded elements in the bucket
     uint64_t per_block;              // slice length, a multiple of the vector width
@@ -232,7 +233,7 @@ struct BucketParams {
     // 1 in every bucket kernel of a call but the first: its blocks load their
     // first vectors before waiting for the previous kernel (see bucket_kernel)
     uint32_t early;
-    uint32_t pad;
+    uint32_t blocks;                 // data blocks (the barrier block comes after them)
     // The signal-window barrier after this bucket, run by one extra block at
     // the end of the grid (win != nullptr; see bucket_kernel): the group's
     // window [P][P], followed by rank_gen[P] and the counter of finished
@@ -250,6 +251,8 @@ constexpr size_t win_words(int P) { return (size_t)P * P + P + 4; }
 uint64_t bucket_padded(uint64_t count, int dtype);
 cudaError_t bucket_grid(int dtype, int op, int P, uint64_t total, int device, uint32_t *blocks,
                         uint64_t *per_block);
+// Blocks (slices of per_block elements) of one tensor of `count` elements.
+uint64_t bucket_tensor_blocks(uint64_t count, int dtype, uint64_t per_block);
 
 // ---- barrier ----------------------------------------------------------------
 struct BarrierParams {

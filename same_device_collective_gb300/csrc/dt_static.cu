@@ -130,6 +130,7 @@ dt_status launch_all(const unsigned char *d, size_t ptr_bytes, size_t tab_bytes,
         bp.ntensors = (uint32_t)(L.te - L.tb);
         bp.total = L.total;
         bp.per_block = L.per_block;
+        bp.blocks = L.blocks;
         bp.early = kernel_before ? 1u : 0u;
         bool launched = false;
         if (dt::launch_bucket(bp, dtype, op, device, s, &launched) != cudaSuccess) return DT_ERR_CUDA;
@@ -210,7 +211,7 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
             tab[t].first = first;
             tab[t].count = counts[t];
             tab[t].slot = (uint32_t)t | (al ? 0x80000000u : 0u);
-            tab[t].pad = 0;
+            tab[t].block0 = 0;   // set below, once the bucket's slice length is known
             first += dt::bucket_padded(counts[t], dtype);
             filled += counts[t] * es;
             ++t;
@@ -223,13 +224,17 @@ extern "C" dt_status dt_bucket_allreduce_static(int world_size, void *const *gra
         L.total = first;
         if (dt::bucket_grid(dtype, op, P, L.total, device, &L.blocks, &L.per_block) != cudaSuccess)
             return DT_ERR_CUDA;
-        if (n_starts + L.blocks > max_starts) return DT_ERR_TOO_LARGE;
+        // one block per slice of a tensor: the grid's slice length, cut at tensor ends
+        uint64_t nblk = 0;
+        for (size_t k = L.tb; k < L.te; ++k) nblk += dt::bucket_tensor_blocks(counts[k], dtype, L.per_block);
+        if (n_starts + nblk > max_starts) return DT_ERR_TOO_LARGE;
+        L.blocks = (uint32_t)nblk;
         L.start_off = n_starts;
-        size_t k = L.tb;
-        for (uint32_t j = 0; j < L.blocks; ++j) {
-            const uint64_t lo = (uint64_t)j * L.per_block;
-            while (k + 1 < L.te && tab[k + 1].first <= lo) ++k;
-            starts[n_starts++] = (uint32_t)(k - L.tb);
+        uint32_t block = 0;
+        for (size_t k = L.tb; k < L.te; ++k) {
+            tab[k].block0 = block;
+            const uint64_t nb_k = dt::bucket_tensor_blocks(counts[k], dtype, L.per_block);
+            for (uint64_t j = 0; j < nb_k; ++j, ++block) starts[n_starts++] = (uint32_t)(k - L.tb);
         }
     }
     if (nl == 0) return DT_OK;
