@@ -27,9 +27,11 @@ struct BucketUnroll {   // 8 loads of 16 bytes in flight per thread (16 at P > 8
 
 // Threads per bucket block.  Blocks make one pass over their slice, so the
 // block size sets the slice and with it how long the last blocks of a bucket
-// run alone at its end: 128 threads measured 384 -> 380 us per call on the
-// 200-gradient, 8-rank workload against 256 (64: no further gain).
-constexpr int kBucketThreads = 128;
+// run alone at its end.  On the 200-gradient, 8-rank workload, with slices cut
+// at tensor ends: 256 threads 363.0 us per call, 192 363.1, 128 364.2, 64
+// 390-408, and two passes of 128 threads 372.7.  (While slices could cross
+// into a second tensor, 128 threads had been best: 380 against 384 at 256.)
+constexpr int kBucketThreads = 256;
 
 // The signal-window barrier between this bucket and the next, run by the
 // grid's extra last block (the page's notify / wait with a generation; the
