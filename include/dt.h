@@ -291,8 +291,8 @@ dt_status dt_barrier(dt_group_t g, int rank, void *stream);
  * this library (every GPU that loads the library holds it until the process
  * exits) and are staged from a fixed host array: the call allocates nothing.
  * Tables that do not fit (n_tensors * (P * 8 + 24) bytes plus 4 bytes per
- * thread block of every bucket: one block per 1024 bf16 or 512 fp32
- * elements of each tensor, at most 16 per resident block slot, so about 20
+ * thread block of every bucket: one block per 2048 bf16 or 1024 fp32
+ * elements of each tensor, at most 16 per resident block slot, so about 40
  * full 25 MiB buckets) or more than 4096 buckets return DT_ERR_TOO_LARGE before anything
  * is enqueued.  Every call shares the array and leaves its contents behind;
  * calls that overlap on the GPU (unordered streams) race on it, calls on one
