@@ -368,6 +368,49 @@ def test_bucket_misaligned_tensor(dt):
         assert_same(host(grads[0][p]), ref[0][p], f"rank {p}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("P", [2, 3, 8])
+def test_bucket_slices_at_tensor_ends(dt, dtype, P):
+    # Every block works on one slice of one tensor: slices of the bucket's
+    # slice length (one pass of the block's threads: 2048 bf16 or 1024 fp32
+    # elements for these sizes) cut at every tensor's end.  Counts around
+    # multiples of that length, empty and one-element tensors, and two
+    # tensors whose ranks are not 16-byte aligned (element path over several
+    # slices) between aligned ones, in one bucket and in many.
+    rng = np.random.default_rng(P * 7 + len(dtype))
+    L = 2048 if dtype == "bf16" else 1024
+    counts = [L, L + 1, L - 1, 1, 0, 2 * L + 7, 3 * L - 1, 8, 9, 3 * L, 5 * L + 3, L // 2]
+    misaligned = {3, 6}
+    for cap in (1, 3 * L * ELEM[dtype], 25 << 20):
+        values = [[torch.from_numpy(rng.standard_normal(c).astype(np.float32)).to(TORCH_DTYPE[dtype])
+                   for _ in range(P)] for c in counts]
+        ref = [[host(v).copy() for v in row] for row in values]
+        oracle.bucket_allreduce(dtype, "avg", ref)
+        for entry in ("group", "static"):
+            grads = []
+            for t, c in enumerate(counts):
+                row = []
+                for p in range(P):
+                    if t in misaligned:
+                        x = offset_view(c, dtype, 1 + p)
+                        x.copy_(values[t][p].cuda())
+                    else:
+                        x = values[t][p].cuda()
+                    row.append(x)
+                grads.append(row)
+            if entry == "group":
+                with group(P) as g:
+                    dt.dt_bucket_allreduce(g, grads, counts, dtype, "avg", bucket_cap_bytes=cap)
+                    torch.cuda.synchronize()
+                    assert dt.dt_group_check(g) == dt.DT_OK
+            else:
+                dt.dt_bucket_allreduce_static(P, grads, counts, dtype, "avg", cap)
+                torch.cuda.synchronize()
+            for t in range(len(counts)):
+                for p in range(P):
+                    assert_same(host(grads[t][p]), ref[t][p], f"{entry} cap={cap} tensor {t} rank {p}")
+
+
 @pytest.mark.parametrize("P", [1, 2, 3, 8, 16])
 def test_barrier_window_matches_oracle(dt, P):
     with group(P) as g:
